@@ -1,0 +1,263 @@
+"""Pins for the fp64 oracle: each check rests on something other than the oracle itself."""
+
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf16_matrix(seed, tag, shape, std=1.0):
+    return oracle.widen_bf16(synth.bf16_normal(seed, tag, shape, std))
+
+
+# ----------------------------------------------------------- the linear
+def test_linear_exact_rational_bruteforce():
+    """y = (x A) B against exact rational arithmetic on tiny bf16 inputs."""
+    x = _bf16_matrix(1, 10, (3, 8))
+    A = _bf16_matrix(1, 11, (8, 4), 0.3)
+    B = _bf16_matrix(1, 12, (4, 6), 0.5)
+    _, y = oracle.lowrank_linear(x, A, B)
+    for m in range(3):
+        for o in range(6):
+            exact = Fraction(0)
+            for j in range(4):
+                tj = sum(Fraction(float(x[m, k])) * Fraction(float(A[k, j])) for k in range(8))
+                exact += tj * Fraction(float(B[j, o]))
+            assert abs(Fraction(float(y[m, o])) - exact) <= abs(exact) * Fraction(1, 10**13) + Fraction(1, 10**300)
+
+
+def test_linear_associativity():
+    """(x A) B == x (A B): the factor pair acts as the rank-r weight W = A B."""
+    x = _bf16_matrix(2, 1, (5, 96))
+    A = _bf16_matrix(2, 2, (96, 16), 0.1)
+    B = _bf16_matrix(2, 3, (16, 40), 0.25)
+    _, y = oracle.lowrank_linear(x, A, B)
+    W = np.einsum("kj,jo->ko", A, B)
+    y2 = np.einsum("mk,ko->mo", x, W)
+    assert np.max(np.abs(y - y2)) <= 1e-12 * np.max(np.abs(y2))
+
+
+def test_linear_special_cases():
+    x = _bf16_matrix(3, 1, (4, 32))
+    A = _bf16_matrix(3, 2, (32, 8), 0.2)
+    B = _bf16_matrix(3, 3, (8, 24), 0.2)
+    # A = I (r = d_in) reduces to one product x B'
+    Bsq = _bf16_matrix(3, 4, (32, 24))
+    _, y = oracle.lowrank_linear(x, np.eye(32), Bsq)
+    assert np.array_equal(y, x @ Bsq)
+    # B = I (r = d_out) reduces to x A
+    _, y = oracle.lowrank_linear(x, A, np.eye(8))
+    assert np.allclose(y, x @ A, rtol=0, atol=1e-13)
+    # one-hot rows pick rows of W = A B
+    W = A @ B
+    for k in (0, 7, 31):
+        e = np.zeros((1, 32))
+        e[0, k] = 1.0
+        _, y = oracle.lowrank_linear(e, A, B)
+        assert np.allclose(y[0], W[k], rtol=0, atol=1e-15)
+    # zero input gives exact zeros
+    t, y = oracle.lowrank_linear(np.zeros((2, 32)), A, B)
+    assert not np.any(t) and not np.any(y)
+    # rows are independent: permuting rows permutes outputs
+    p = np.array([2, 0, 3, 1])
+    _, y = oracle.lowrank_linear(x, A, B)
+    _, yp = oracle.lowrank_linear(x[p], A, B)
+    assert np.array_equal(yp, y[p])
+
+
+def test_svd_factors_reproduce_rank_r_weight():
+    """A dense W of rank r, split by SVD into (U S, V^T), gives the same layer output."""
+    rng = np.random.default_rng(5)
+    d_in, d_out, r = 48, 40, 6
+    W = rng.normal(size=(d_in, r)) @ rng.normal(size=(r, d_out))
+    U, s, Vt = np.linalg.svd(W)
+    assert np.all(s[r:] <= 1e-10 * s[0])
+    A = U[:, :r] * s[:r]
+    B = Vt[:r]
+    x = rng.normal(size=(7, d_in))
+    _, y = oracle.lowrank_linear(x, A, B)
+    ref = x @ W
+    assert np.max(np.abs(y - ref)) <= 1e-10 * np.max(np.abs(ref))
+    # Eckart-Young: truncating to k < r leaves exactly the tail energy
+    k = 3
+    Wk = (U[:, :k] * s[:k]) @ Vt[:k]
+    assert abs(np.linalg.norm(W - Wk) ** 2 - np.sum(s[k:] ** 2)) <= 1e-8 * np.sum(s ** 2)
+
+
+# ------------------------------------------------------------- the rank rule
+def test_rank_table():
+    with open(os.path.join(GOLDEN, "rank_table.json")) as f:
+        rows = json.load(f)["rows"]
+    for d_in, d_out, rho, r in rows:
+        assert oracle.rank_for(d_in, d_out, rho) == r, (d_in, d_out, rho)
+
+
+# --------------------------------------------------------------- the glue
+def test_rmsnorm_closed_forms():
+    # [3, 4] with eps = 0: mean square 12.5, so [3, 4] / sqrt(12.5)
+    y = oracle.rmsnorm(np.array([[3.0, 4.0]]), eps=0.0)
+    assert np.allclose(y, [[0.848528137423857, 1.131370849898476]], rtol=1e-15)
+    # a constant row c: c / sqrt(c^2 + eps)
+    c = 0.01
+    y = oracle.rmsnorm(np.full((1, 64), c), eps=1e-6)
+    assert np.allclose(y, 0.01 / np.sqrt(1e-4 + 1e-6), rtol=1e-15)
+    # positive scale invariance when eps = 0; mean square of the output is 1
+    h = _bf16_matrix(4, 1, (3, 256))
+    assert np.allclose(oracle.rmsnorm(7.5 * h, eps=0.0), oracle.rmsnorm(h, eps=0.0), rtol=1e-14)
+    assert np.allclose(np.mean(oracle.rmsnorm(h, eps=0.0) ** 2, axis=1), 1.0, rtol=1e-14)
+
+
+def test_silu_identities():
+    z = np.linspace(-20, 20, 401)
+    s = oracle.silu(z)
+    assert oracle.silu(np.array([0.0]))[0] == 0.0
+    # z*sig(z) - (-z)*sig(-z) = z since sig(z) + sig(-z) = 1
+    assert np.allclose(s - oracle.silu(-z), z, rtol=0, atol=1e-13)
+    # silu(ln 3) = ln3 * 3/4 (sigmoid(ln 3) = 3/4)
+    assert np.isclose(oracle.silu(np.array([np.log(3.0)]))[0], 0.75 * np.log(3.0), rtol=1e-15)
+    assert np.all(np.abs(s[z > 15] - z[z > 15]) < 1e-5)
+    assert np.all(np.abs(s[z < -15]) < 1e-5)
+
+
+def _softmax_attention_one_key(q, k, v, n_heads, n_kv, hd):
+    """Textbook scaled-dot-product attention over a context of one token."""
+    M = q.shape[0]
+    g = n_heads // n_kv
+    out = np.zeros((M, n_heads * hd))
+    for m in range(M):
+        for h in range(n_heads):
+            kvh = h // g
+            qh = q[m, h * hd:(h + 1) * hd]
+            kh = k[m, kvh * hd:(kvh + 1) * hd]
+            scores = np.array([qh @ kh / np.sqrt(hd)])
+            w = np.exp(scores - scores.max())
+            w /= w.sum()
+            out[m, h * hd:(h + 1) * hd] = w[0] * v[m, kvh * hd:(kvh + 1) * hd]
+    return out
+
+
+@pytest.mark.parametrize("n_heads,n_kv", [(4, 4), (8, 2), (4, 1)])
+def test_one_token_attention_is_softmax_attention(n_heads, n_kv):
+    hd = 8
+    q = _bf16_matrix(6, 1, (3, n_heads * hd))
+    k = _bf16_matrix(6, 2, (3, n_kv * hd))
+    v = _bf16_matrix(6, 3, (3, n_kv * hd))
+    got = oracle.one_token_attention(v, n_heads, n_kv, hd)
+    ref = _softmax_attention_one_key(q, k, v, n_heads, n_kv, hd)
+    assert np.array_equal(got, ref)
+
+
+def _zero_factors(d, d_kv, dff, r=8):
+    z = lambda a, b: (np.zeros((a, r)), np.zeros((r, b)))
+    return {"q": z(d, d), "k": z(d, d_kv), "v": z(d, d_kv), "o": z(d, d),
+            "gate": z(d, dff), "up": z(d, dff), "down": z(dff, d)}
+
+
+def test_block_zero_factors_is_identity():
+    h = _bf16_matrix(7, 1, (3, 32))
+    f = _zero_factors(32, 16, 48)
+    assert np.array_equal(oracle.block_forward(h, f, 4, 2, 8), h)
+    assert np.array_equal(oracle.stack_forward(h, [f, f, f], 4, 2, 8), h)
+
+
+def test_block_attention_path_bruteforce():
+    """v = n1[:, :d_kv] and o = I: h1 = h + GQA-broadcast of n1 columns, by index loops."""
+    d, n_heads, n_kv, hd = 32, 4, 2, 8
+    d_kv = n_kv * hd
+    h = _bf16_matrix(8, 1, (2, d))
+    f = _zero_factors(d, d_kv, 48)
+    f["v"] = (np.eye(d)[:, :d_kv], np.eye(d_kv))
+    f["o"] = (np.eye(d), np.eye(d))
+    out = oracle.block_forward(h, f, n_heads, n_kv, hd, eps=1e-6, return_all=True)
+    n1 = h / np.sqrt(np.mean(h ** 2, axis=1, keepdims=True) + 1e-6)
+    want = h.copy()
+    for m in range(2):
+        for c in range(d):
+            head, e = divmod(c, hd)
+            kvh = head // (n_heads // n_kv)
+            want[m, c] += n1[m, kvh * hd + e]
+    assert np.allclose(out["h1"], want, rtol=0, atol=1e-14)
+    # MLP factors are zero, so the block output is h1
+    assert np.array_equal(out["h2"], out["h1"])
+
+
+def test_block_mlp_path():
+    """gate = up = n2 and down = I: h2 = h1 + silu(n2) * n2."""
+    d = 16
+    h = _bf16_matrix(9, 1, (2, d))
+    f = _zero_factors(d, d, d)
+    f["gate"] = (np.eye(d), np.eye(d))
+    f["up"] = (np.eye(d), np.eye(d))
+    f["down"] = (np.eye(d), np.eye(d))
+    out = oracle.block_forward(h, f, 2, 2, 8, return_all=True)
+    n2 = out["n2"]
+    want = h + (n2 / (1 + np.exp(-n2))) * n2
+    assert np.allclose(out["h2"], want, rtol=0, atol=1e-14)
+
+
+def test_stack_is_composition():
+    d, dff = 32, 48
+    h = _bf16_matrix(10, 1, (3, d))
+    layers = []
+    for l in range(2):
+        f = {}
+        for p, (a, b) in zip(synth.PROJ_NAMES,
+                             [(d, d), (d, 16), (d, 16), (d, d), (d, dff), (d, dff), (dff, d)]):
+            f[p] = (_bf16_matrix(11, 100 * l + 2 * len(f), (a, 8), a ** -0.5),
+                    _bf16_matrix(11, 100 * l + 2 * len(f) + 1, (8, b), 8 ** -0.5))
+        layers.append(f)
+    s = oracle.stack_forward(h, layers, 4, 2, 8)
+    b = oracle.block_forward(oracle.block_forward(h, layers[0], 4, 2, 8), layers[1], 4, 2, 8)
+    assert np.array_equal(s, b)
+
+
+# -------------------------------------------------------------- the remap
+def test_remap_build_golden():
+    with open(os.path.join(GOLDEN, "remap_build_small.json")) as f:
+        g = json.load(f)
+    for c in g["cases"]:
+        remap, n_active, n_runs = oracle.remap_build(g["lengths"], g["block_table"],
+                                                     g["block_rows"], c["tail_rows"], c["cap"])
+        assert remap.tolist() == c["remap"]
+        assert n_active == c["n_active"]
+        assert n_runs == c["n_runs"]
+    with pytest.raises(ValueError):
+        oracle.remap_build(g["lengths"], g["block_table"], g["block_rows"], 0, 17)
+
+
+def test_remap_permutation_inverse():
+    pool = synth.bf16_normal(0, 77, (40, 24))
+    p = synth.permutation(0, 78, 40)[:16]           # 16 distinct pool rows
+    buf, bad = oracle.remap_gather(pool, p, 16, 20)
+    assert not bad
+    assert np.array_equal(buf[:16], pool[p])
+    assert not np.any(buf[16:])
+    # scatter of the gathered rows restores the pool exactly
+    back, bad = oracle.remap_scatter(buf, p, 16, np.zeros_like(pool))
+    assert not bad
+    assert np.array_equal(back[p], pool[p])
+    mask = np.ones(40, bool)
+    mask[p] = False
+    assert not np.any(back[mask])
+    # gather with the inverse permutation undoes a full permutation
+    q = synth.permutation(0, 79, 40)
+    inv = np.argsort(q)
+    once, _ = oracle.remap_gather(pool, q, 40, 40)
+    twice, _ = oracle.remap_gather(once, inv, 40, 40)
+    assert np.array_equal(twice, pool)
+
+
+def test_remap_out_of_range_and_padding():
+    pool = synth.bf16_normal(0, 80, (8, 4))
+    buf, bad = oracle.remap_gather(pool, [3, 99, -1, 0], 3, 5)
+    assert bad
+    assert np.array_equal(buf[0], pool[3])
+    assert not np.any(buf[1]) and not np.any(buf[2])   # bad entries give zero rows
+    assert not np.any(buf[3:])                         # rows >= n_active are zero
