@@ -1,0 +1,217 @@
+/*
+ * lr.h -- C ABI of liblr, the GB300 (sm_103a) factorized-linear inference path.
+ *
+ * What it computes comes from DeInfer: Efficient Parallel Inferencing for
+ * Decomposed Large Language Models (Huang, Huang, Liao, Wen), as summarised on
+ * gist.science/paper/2604.17709 (English page) and gist.science/es/paper/
+ * 2604.17709 (Spanish page).  Every weight W[d_in][d_out] of a transformer
+ * block is approximated by two low-rank factors, W ~ A_r B_r (Spanish page,
+ * "Resumen Tecnico" section 1; English page section 1), and a layer is
+ * evaluated as a down projection followed by an up projection (English page
+ * section 2.A).  For decoding under a static CUDA graph, rows scattered over
+ * paged memory are first listed in a remap table and copied into a fixed
+ * buffer; the graph then runs fixed-size GEMMs on that buffer (English page
+ * section 2.C).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers marked "device" are CUDA device pointers owned by the caller; the
+ *   library never allocates, frees or keeps them past the call (the graph
+ *   object keeps them, see lr_graph_capture).  Pointers marked "host" are
+ *   ordinary host memory.
+ * - bf16 means IEEE bfloat16 bit patterns (uint16_t).  All matrices are
+ *   row-major with the leading dimension given in elements.
+ * - Factors are stored out-major, the layout of a linear layer's weight:
+ *   the down factor A_r[d_in][r] is stored transposed as At[r][d_in] and the
+ *   up factor B_r[r][d_out] as Bt[d_out][r].  Every tensor-core operand is
+ *   then contiguous along the reduction dimension.
+ * - Work is enqueued on the given stream (0 = the legacy default stream) and
+ *   runs asynchronously.  Argument errors are detected on the host before
+ *   anything is enqueued and returned as LR_ERR_INVALID_ARG or
+ *   LR_ERR_UNSUPPORTED; nothing is launched in that case.
+ * - Device-side problems never trap: a kernel that meets one stores the first
+ *   error code into the caller's int32 device word `dev_status` (compare-and-
+ *   swap from 0) and finishes safely.  The caller reads it after synchronising
+ *   and resets it to 0.
+ * - Every wait inside a kernel is bounded (about two seconds); a wait that
+ *   runs out reports LR_ERR_TIMEOUT through dev_status and the kernel returns.
+ * - No exception crosses this interface.  lr_last_error() gives a one-line
+ *   description of the last host-side error of the calling thread.
+ */
+#ifndef LR_H_
+#define LR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* lr_stream; /* a cudaStream_t */
+
+typedef enum {
+  LR_OK = 0,
+  LR_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, small buffer */
+  LR_ERR_UNSUPPORTED = 2,  /* a dimension outside what the kernels handle */
+  LR_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+  LR_ERR_TIMEOUT = 4,      /* device: a bounded wait ran out */
+  LR_ERR_REMAP_RANGE = 5,  /* device: a remap entry outside the pool */
+  LR_ERR_STATE = 6         /* wrong object state (e.g. replaying a destroyed graph) */
+} lr_status;
+
+typedef enum { LR_BF16 = 0, LR_F32 = 1 } lr_dtype;
+
+/* One factor pair (A_r, B_r) of a decomposed projection, W ~ A_r B_r.
+ * At: device bf16 [r][d_in]  (A_r transposed), row stride d_in.
+ * Bt: device bf16 [d_out][r] (B_r transposed), row stride r.
+ * d_in, d_out and r must be positive multiples of 64 (LR_ERR_UNSUPPORTED
+ * otherwise); both pointers must be 16-byte aligned. */
+typedef struct {
+  const void* At;
+  const void* Bt;
+  int32_t d_in;
+  int32_t d_out;
+  int32_t r;
+} lr_factor;
+
+/* Projections of a block, in this order (English page section 2.D: attention
+ * and MLP projections are all decomposed). */
+enum { LR_Q = 0, LR_K = 1, LR_V = 2, LR_O = 3, LR_GATE = 4, LR_UP = 5, LR_DOWN = 6 };
+
+/* A decomposed LLaMA-style block whose attention core is attention over a
+ * one-token context (each query head returns the value vector of its kv head).
+ * q: d_model -> n_heads*head_dim, k/v: d_model -> n_kv_heads*head_dim,
+ * o: n_heads*head_dim -> d_model, gate/up: d_model -> d_ff, down: d_ff -> d_model.
+ * n_heads must be a multiple of n_kv_heads (MHA, GQA, MQA); head_dim a multiple
+ * of 64; RMSNorm has unit gain and the given eps. */
+typedef struct {
+  int32_t d_model;
+  int32_t d_ff;
+  int32_t n_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  float eps;
+  lr_factor f[7];
+} lr_block_desc;
+
+/* ---------------------------------------------------------------------------
+ * lr_linear_forward: y = (x A_r) B_r for M rows.
+ * English page section 2.A (down projection, then up projection); Spanish
+ * page "Resumen Tecnico" section 1 (W ~ A B).
+ *   x  device bf16 [M][ldx], ldx >= d_in, ldx multiple of 8, x 16-byte aligned.
+ *   y  device [M][ldy] of y_dtype (LR_BF16 or LR_F32), ldy >= d_out.
+ *   The intermediate t = x A_r is rounded to bf16 (round to nearest even) and
+ *   kept in `workspace`; the sums accumulate in fp32.  A bf16 y is the
+ *   round-to-nearest-even image of the fp32 y.
+ *   workspace: device, at least lr_linear_workspace_bytes(M, f) bytes, 256-byte
+ *   aligned, zero-filled before its first use; the kernels leave it reusable.
+ *   Calls that share a workspace must be ordered on one stream.
+ *   M = 0 is a no-op.  M <= 256 runs the decode kernels, larger M the prefill
+ *   kernels.  The result is deterministic (no floating-point atomics). */
+size_t lr_linear_workspace_bytes(int64_t M, const lr_factor* f);
+lr_status lr_linear_forward(const void* x, int64_t ldx, void* y, int64_t ldy, lr_dtype y_dtype,
+                            int64_t M, const lr_factor* f, void* workspace, size_t ws_bytes,
+                            int32_t* dev_status, lr_stream s);
+
+/* ---------------------------------------------------------------------------
+ * lr_block_forward: one decomposed block applied in place to the fp32 residual
+ * stream h (device fp32 [M][d_model], 16-byte aligned):
+ *   n1 = RMSNorm(h); q,k,v = LR(n1); h += LR_o(attn(v));
+ *   n2 = RMSNorm(h); h += LR_down(silu(LR_gate(n2)) * LR_up(n2)).
+ * Spanish page section 1 (attention and MLP projections decomposed) and
+ * section 2 "Generalizacion"; English page section 2.D (MHA/GQA/MQA, GLU MLP).
+ * Linear inputs are rounded to bf16.  scratch: device, at least
+ * lr_block_scratch_bytes(M, b) bytes, 256-byte aligned, zero-filled before its
+ * first use.  M = 0 is a no-op. */
+size_t lr_block_scratch_bytes(int64_t M, const lr_block_desc* b);
+lr_status lr_block_forward(float* h, int64_t M, const lr_block_desc* b, void* scratch,
+                           size_t scratch_bytes, int32_t* dev_status, lr_stream s);
+
+/* ---------------------------------------------------------------------------
+ * remap_compact: the copy of the preparation stage (English page section 2.C):
+ *   buf[i][:] = pool[remap[i]][:] for 0 <= i < min(*n_active, cap), zero rows
+ *   for i >= *n_active.  Bit-exact byte copy of row_bytes per row.
+ *   pool: device [pool_rows][row_bytes]; buf: device [cap][row_bytes];
+ *   remap: device int32 [cap]; n_active: device int32 (read on the device, so
+ *   the launch parameters never change with the batch).  row_bytes must be a
+ *   positive multiple of 16 and every pointer 16-byte aligned.  An entry
+ *   outside [0, pool_rows) gives a zero row and LR_ERR_REMAP_RANGE in
+ *   dev_status. */
+lr_status remap_compact(const void* pool, int64_t pool_rows, int64_t row_bytes,
+                        const int32_t* remap, const int32_t* n_active, void* buf, int64_t cap,
+                        int32_t* dev_status, lr_stream s);
+
+/* remap_scatter: the inverse copy, pool[remap[i]][:] = buf[i][:] for
+ * 0 <= i < min(*n_active, cap).  Same arguments and checks as remap_compact;
+ * an out-of-range entry is skipped and reported.  Targets must be distinct
+ * (remap_build makes them so); with duplicates the surviving row is
+ * unspecified. */
+lr_status remap_scatter(const void* buf, const int32_t* remap, const int32_t* n_active,
+                        void* pool, int64_t pool_rows, int64_t row_bytes, int64_t cap,
+                        int32_t* dev_status, lr_stream s);
+
+/* remap_build (host only): the scan of the preparation stage (English page
+ * section 2.C, "remapping index list (a new block table)").
+ *   lengths: host int32 [n_seq]; block_table: host int32 [n_seq][blocks_per_seq],
+ *   entry (s, b) = physical block of logical block b of sequence s.
+ *   For each sequence in order, its last tail_rows positions (all positions if
+ *   tail_rows <= 0) are mapped to physical rows
+ *   block_table[s][p / block_rows] * block_rows + p % block_rows.
+ *   Outputs (host): remap_out[cap] (unused entries -1), *n_active_out, and
+ *   *n_runs_out = number of maximal runs of consecutive physical rows.
+ *   LR_ERR_INVALID_ARG if the rows exceed cap, a needed table entry is
+ *   negative, a length is negative or exceeds the table, or two rows coincide. */
+lr_status remap_build(const int32_t* lengths, int64_t n_seq, const int32_t* block_table,
+                      int32_t blocks_per_seq, int32_t block_rows, int32_t tail_rows, int64_t cap,
+                      int32_t* remap_out, int32_t* n_active_out, int32_t* n_runs_out);
+
+/* ---------------------------------------------------------------------------
+ * A decode step of a layer stack over fixed buffers (English page section 2.C:
+ * addresses and launch parameters stay fixed while the logical batch changes):
+ *   xbuf = remap_compact(pool_in); h = widen(xbuf); for each layer:
+ *   lr_block_forward(h, cap rows); ybuf = bf16(h); remap_scatter(ybuf -> pool_out).
+ * pool_in/pool_out: device bf16 [pool_rows][d_model] (may be the same buffer);
+ * xbuf/ybuf: device bf16 [cap][d_model]; h: device fp32 [cap][d_model];
+ * scratch: max over layers of lr_block_scratch_bytes(cap, layer).
+ * All layers must share d_model.  Rows i >= *n_active run through the layers
+ * as zero rows and are not scattered. */
+typedef struct {
+  int32_t n_layers;
+  const lr_block_desc* layers; /* host array [n_layers]; copied by the calls */
+  const void* pool_in;
+  void* pool_out;
+  int64_t pool_rows;
+  const int32_t* remap;
+  const int32_t* n_active;
+  int64_t cap;
+  void* xbuf;
+  float* h;
+  void* ybuf;
+  void* scratch;
+  size_t scratch_bytes;
+  int32_t* dev_status;
+} lr_stack_desc;
+
+/* Enqueue one step eagerly (one launch per kernel). */
+lr_status lr_stack_forward(const lr_stack_desc* st, lr_stream s);
+
+/* Capture one step into a CUDA graph owned by the library (captured on a
+ * private stream; the caller's streams are not touched).  The graph keeps the
+ * descriptor's device pointers: they must stay valid until lr_graph_destroy.
+ * Per step only the contents of remap, *n_active and the pool change. */
+typedef struct lr_graph lr_graph;
+lr_status lr_graph_capture(const lr_stack_desc* st, lr_graph** out);
+lr_status lr_graph_replay(lr_graph* g, lr_stream s);
+lr_status lr_graph_destroy(lr_graph* g);
+
+/* Number of kernel launches one step enqueues (eager or in the graph). */
+int64_t lr_stack_launch_count(const lr_stack_desc* st);
+
+const char* lr_status_string(lr_status st);
+const char* lr_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LR_H_ */

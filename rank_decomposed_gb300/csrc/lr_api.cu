@@ -1,0 +1,553 @@
+// Host side of liblr: argument validation, tensor-map encoding, the order of
+// kernels inside a decomposed linear, a block and a layer stack, the remap
+// scan, and CUDA-graph capture/replay.  See include/lr.h for the contract.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "lr_internal.h"
+
+namespace lr {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+lr_status cuda_fail(cudaError_t e, const char* what) {
+  set_error("%s: %s", what, cudaGetErrorString(e));
+  return LR_ERR_CUDA;
+}
+
+static lr_status invalid_device() {
+  set_error("device ordinal outside the supported range");
+  return LR_ERR_UNSUPPORTED;
+}
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("LR_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
+// cuTensorMapEncodeTiled, looked up once through the runtime so the library
+// needs no link-time dependency on the driver library.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+lr_status encode_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                          uint64_t ld, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) {
+    set_error("cuTensorMapEncodeTiled unavailable");
+    return LR_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d): rows=%llu cols=%llu ld=%llu box_rows=%u",
+              static_cast<int>(r), (unsigned long long)rows, (unsigned long long)cols,
+              (unsigned long long)ld, box_rows);
+    return LR_ERR_CUDA;
+  }
+  return LR_OK;
+}
+
+lr_status ensure_configured() {
+  static bool done[64] = {false};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return invalid_device();
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return LR_OK;
+  lr_status st = configure_decode();
+  if (st != LR_OK) return st;
+  st = configure_prefill();
+  if (st != LR_OK) return st;
+  done[dev] = true;
+  return LR_OK;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+lr_status invalid(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return LR_ERR_INVALID_ARG;
+}
+
+lr_status check_factor(const lr_factor* f, const char* name) {
+  if (f == nullptr) return invalid("%s: null factor", name);
+  if (f->d_in <= 0 || f->d_out <= 0 || f->r <= 0) return invalid("%s: non-positive dims", name);
+  if (f->d_in % 64 || f->d_out % 64 || f->r % 64) {
+    set_error("%s: d_in=%d d_out=%d r=%d must be multiples of 64", name, f->d_in, f->d_out, f->r);
+    return LR_ERR_UNSUPPORTED;
+  }
+  if (f->At == nullptr || f->Bt == nullptr) return invalid("%s: null factor pointer", name);
+  if (!aligned16(f->At) || !aligned16(f->Bt)) return invalid("%s: factors not 16-byte aligned", name);
+  return LR_OK;
+}
+
+GemmOp make_op(const void* W, int N, int K, const void* act, int64_t ld_act, int64_t act_cols,
+               int epi, void* out, int64_t ldo) {
+  GemmOp o;
+  memset(&o, 0, sizeof(o));
+  o.W = W;
+  o.N = N;
+  o.K = K;
+  o.ldw = K;
+  o.act = act;
+  o.ld_act = ld_act;
+  o.act_cols = act_cols;
+  o.epi = epi;
+  o.out = out;
+  o.ldo = ldo;
+  return o;
+}
+
+// Run a group of ops that share M: one grouped launch for decode sizes, one
+// launch per op for prefill sizes.
+lr_status run_ops(int64_t M, const GemmOp* ops, int n, int32_t* status, cudaStream_t s) {
+  lr_status cst = ensure_configured();
+  if (cst != LR_OK) return cst;
+  if (M <= kDecodeMaxRows) return launch_decode(static_cast<int>(M), ops, n, status, s);
+  for (int i = 0; i < n; ++i) {
+    lr_status st = launch_prefill(M, ops[i], status, s);
+    if (st != LR_OK) return st;
+  }
+  return LR_OK;
+}
+
+// ---------------------------------------------------------------- block
+struct BlockLayout {
+  size_t n1, t[7], q, k, v, n2, g, u, a, total;
+};
+
+BlockLayout block_layout(int64_t M, const lr_block_desc* b) {
+  BlockLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += align_up(bytes);
+    return o;
+  };
+  const size_t m = static_cast<size_t>(M);
+  L.n1 = take(m * b->d_model * 2);
+  for (int i = 0; i < 7; ++i) L.t[i] = take(m * b->f[i].r * 2);
+  L.q = take(m * b->f[LR_Q].d_out * 2);
+  L.k = take(m * b->f[LR_K].d_out * 2);
+  L.v = take(m * b->f[LR_V].d_out * 2);
+  L.n2 = take(m * b->d_model * 2);
+  L.g = take(m * b->d_ff * 2);
+  L.u = take(m * b->d_ff * 2);
+  L.a = take(m * b->d_ff * 2);
+  L.total = off;
+  return L;
+}
+
+lr_status check_block(const lr_block_desc* b) {
+  if (b == nullptr) return invalid("block: null descriptor");
+  static const char* names[7] = {"q", "k", "v", "o", "gate", "up", "down"};
+  for (int i = 0; i < 7; ++i) {
+    lr_status st = check_factor(&b->f[i], names[i]);
+    if (st != LR_OK) return st;
+  }
+  const int d = b->d_model, dff = b->d_ff, hd = b->head_dim;
+  if (d <= 0 || dff <= 0 || hd <= 0 || b->n_heads <= 0 || b->n_kv_heads <= 0)
+    return invalid("block: non-positive shape");
+  if (b->n_heads % b->n_kv_heads) return invalid("block: n_heads %% n_kv_heads != 0");
+  if (hd % 64 || d % 64 || dff % 64) {
+    set_error("block: d_model, d_ff and head_dim must be multiples of 64");
+    return LR_ERR_UNSUPPORTED;
+  }
+  if (!(b->eps >= 0.f)) return invalid("block: eps must be >= 0");
+  const int dq = b->n_heads * hd, dkv = b->n_kv_heads * hd;
+  const int want[7][2] = {{d, dq}, {d, dkv}, {d, dkv}, {dq, d}, {d, dff}, {d, dff}, {dff, d}};
+  for (int i = 0; i < 7; ++i)
+    if (b->f[i].d_in != want[i][0] || b->f[i].d_out != want[i][1])
+      return invalid("block: factor %s is %dx%d, expected %dx%d", names[i], b->f[i].d_in,
+                     b->f[i].d_out, want[i][0], want[i][1]);
+  return LR_OK;
+}
+
+lr_status enqueue_block(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws,
+                        int32_t* status, cudaStream_t s) {
+  const BlockLayout L = block_layout(M, b);
+  const int d = b->d_model, dff = b->d_ff;
+  const lr_factor* f = b->f;
+  void* t[7];
+  for (int i = 0; i < 7; ++i) t[i] = ws + L.t[i];
+  void* n1 = ws + L.n1;
+  void* n2 = ws + L.n2;
+  lr_status st;
+#define LR_TRY(x)          \
+  do {                     \
+    st = (x);              \
+    if (st != LR_OK) return st; \
+  } while (0)
+  // attention half: n1 = RMSNorm(h); q, k, v = LR(n1); h += LR_o(attn(v))
+  LR_TRY(launch_rmsnorm(h, n1, M, d, b->eps, s));
+  {
+    GemmOp down[3], up[3];
+    void* outs[3] = {ws + L.q, ws + L.k, ws + L.v};
+    for (int i = 0; i < 3; ++i) {
+      down[i] = make_op(f[i].At, f[i].r, d, n1, d, d, EPI_STORE_BF16, t[i], f[i].r);
+      up[i] = make_op(f[i].Bt, f[i].d_out, f[i].r, t[i], f[i].r, f[i].r, EPI_STORE_BF16, outs[i],
+                      f[i].d_out);
+    }
+    LR_TRY(run_ops(M, down, 3, status, s));
+    LR_TRY(run_ops(M, up, 3, status, s));
+  }
+  {
+    const int dq = b->n_heads * b->head_dim, dkv = b->n_kv_heads * b->head_dim;
+    GemmOp od = make_op(f[LR_O].At, f[LR_O].r, dq, ws + L.v, dkv, dkv, EPI_STORE_BF16, t[LR_O],
+                        f[LR_O].r);
+    if (b->n_heads != b->n_kv_heads) {
+      od.gqa_head_dim = b->head_dim;
+      od.gqa_group = b->n_heads / b->n_kv_heads;
+    }
+    GemmOp ou = make_op(f[LR_O].Bt, d, f[LR_O].r, t[LR_O], f[LR_O].r, f[LR_O].r, EPI_ADD_F32, h, d);
+    LR_TRY(run_ops(M, &od, 1, status, s));
+    LR_TRY(run_ops(M, &ou, 1, status, s));
+  }
+  // MLP half: n2 = RMSNorm(h); h += LR_down(silu(LR_gate(n2)) * LR_up(n2))
+  LR_TRY(launch_rmsnorm(h, n2, M, d, b->eps, s));
+  {
+    GemmOp down[2], up[2];
+    void* outs[2] = {ws + L.g, ws + L.u};
+    for (int i = 0; i < 2; ++i) {
+      const lr_factor& fi = f[LR_GATE + i];
+      down[i] = make_op(fi.At, fi.r, d, n2, d, d, EPI_STORE_BF16, t[LR_GATE + i], fi.r);
+      up[i] = make_op(fi.Bt, dff, fi.r, t[LR_GATE + i], fi.r, fi.r, EPI_STORE_BF16, outs[i], dff);
+    }
+    LR_TRY(run_ops(M, down, 2, status, s));
+    LR_TRY(run_ops(M, up, 2, status, s));
+  }
+  LR_TRY(launch_silu_mul(ws + L.g, ws + L.u, ws + L.a, M, dff, s));
+  {
+    const lr_factor& fd = f[LR_DOWN];
+    GemmOp dd = make_op(fd.At, fd.r, dff, ws + L.a, dff, dff, EPI_STORE_BF16, t[LR_DOWN], fd.r);
+    GemmOp du = make_op(fd.Bt, d, fd.r, t[LR_DOWN], fd.r, fd.r, EPI_ADD_F32, h, d);
+    LR_TRY(run_ops(M, &dd, 1, status, s));
+    LR_TRY(run_ops(M, &du, 1, status, s));
+  }
+#undef LR_TRY
+  return LR_OK;
+}
+
+int64_t block_launches(int64_t M, const lr_block_desc*) {
+  // rmsnorm x2, silu_mul, and the GEMM launches.
+  if (M <= kDecodeMaxRows) return 3 + 8;
+  return 3 + 14;
+}
+
+// ---------------------------------------------------------------- stack
+lr_status check_stack(const lr_stack_desc* st) {
+  if (st == nullptr) return invalid("stack: null descriptor");
+  if (st->n_layers < 0 || (st->n_layers > 0 && st->layers == nullptr))
+    return invalid("stack: bad layer array");
+  if (st->n_layers == 0) return invalid("stack: no layers");
+  if (st->cap <= 0 || st->cap > kDecodeMaxRows * 64) return invalid("stack: bad cap");
+  if (!st->pool_in || !st->pool_out || !st->remap || !st->n_active || !st->xbuf || !st->h ||
+      !st->ybuf || !st->scratch)
+    return invalid("stack: null pointer");
+  if (!aligned16(st->pool_in) || !aligned16(st->pool_out) || !aligned16(st->xbuf) ||
+      !aligned16(st->h) || !aligned16(st->ybuf) || (reinterpret_cast<uintptr_t>(st->scratch) % kAlign))
+    return invalid("stack: misaligned buffer");
+  if (st->pool_rows <= 0) return invalid("stack: empty pool");
+  const int d = st->layers[0].d_model;
+  size_t need = 0;
+  for (int l = 0; l < st->n_layers; ++l) {
+    lr_status s2 = check_block(&st->layers[l]);
+    if (s2 != LR_OK) return s2;
+    if (st->layers[l].d_model != d) return invalid("stack: layers disagree on d_model");
+    need = std::max(need, block_layout(st->cap, &st->layers[l]).total);
+  }
+  if (st->scratch_bytes < need) return invalid("stack: scratch %zu < %zu bytes", st->scratch_bytes, need);
+  return LR_OK;
+}
+
+lr_status enqueue_stack(const lr_stack_desc* st, cudaStream_t s) {
+  const int d = st->layers[0].d_model;
+  const int64_t row_bytes = static_cast<int64_t>(d) * 2;
+  lr_status r = launch_gather(st->pool_in, st->pool_rows, row_bytes, st->remap, st->n_active,
+                              st->xbuf, st->cap, st->dev_status, s);
+  if (r != LR_OK) return r;
+  r = launch_widen(st->xbuf, st->h, st->cap * d, s);
+  if (r != LR_OK) return r;
+  for (int l = 0; l < st->n_layers; ++l) {
+    r = enqueue_block(st->h, st->cap, &st->layers[l], static_cast<uint8_t*>(st->scratch),
+                      st->dev_status, s);
+    if (r != LR_OK) return r;
+  }
+  r = launch_narrow(st->h, st->ybuf, st->cap * d, s);
+  if (r != LR_OK) return r;
+  return launch_scatter(st->ybuf, st->remap, st->n_active, st->pool_out, st->pool_rows,
+                        row_bytes, st->cap, st->dev_status, s);
+}
+
+}  // namespace
+}  // namespace lr
+
+struct lr_graph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  uint32_t magic = 0x4C524750u;
+};
+
+using namespace lr;
+
+extern "C" {
+
+const char* lr_status_string(lr_status st) {
+  switch (st) {
+    case LR_OK: return "ok";
+    case LR_ERR_INVALID_ARG: return "invalid argument";
+    case LR_ERR_UNSUPPORTED: return "unsupported shape";
+    case LR_ERR_CUDA: return "CUDA error";
+    case LR_ERR_TIMEOUT: return "device wait timed out";
+    case LR_ERR_REMAP_RANGE: return "remap entry outside the pool";
+    case LR_ERR_STATE: return "bad object state";
+  }
+  return "unknown status";
+}
+
+const char* lr_last_error(void) { return g_err; }
+
+size_t lr_linear_workspace_bytes(int64_t M, const lr_factor* f) {
+  if (f == nullptr || M < 0) return 0;
+  return align_up(static_cast<size_t>(M) * static_cast<size_t>(f->r) * 2);
+}
+
+lr_status lr_linear_forward(const void* x, int64_t ldx, void* y, int64_t ldy, lr_dtype y_dtype,
+                            int64_t M, const lr_factor* f, void* workspace, size_t ws_bytes,
+                            int32_t* dev_status, lr_stream s) {
+  lr_status st = check_factor(f, "linear");
+  if (st != LR_OK) return st;
+  if (M < 0 || M > (int64_t(1) << 31) - 1) return invalid("linear: bad M");
+  if (M == 0) return LR_OK;
+  if (x == nullptr || y == nullptr || workspace == nullptr) return invalid("linear: null pointer");
+  if (y_dtype != LR_BF16 && y_dtype != LR_F32) return invalid("linear: bad y dtype");
+  if (ldx < f->d_in || ldx % 8 || !aligned16(x)) return invalid("linear: x must be 16-byte aligned with ldx >= d_in, ldx %% 8 == 0");
+  if (ldy < f->d_out) return invalid("linear: ldy < d_out");
+  if (M > kDecodeMaxRows && (!aligned16(y) || ldy % 8)) return invalid("linear: y must be 16-byte aligned with ldy %% 8 == 0");
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return invalid("linear: workspace not 256-byte aligned");
+  if (ws_bytes < lr_linear_workspace_bytes(M, f)) return invalid("linear: workspace too small");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+  GemmOp down = make_op(f->At, f->r, f->d_in, x, ldx, f->d_in, EPI_STORE_BF16, workspace, f->r);
+  GemmOp up = make_op(f->Bt, f->d_out, f->r, workspace, f->r, f->r,
+                      y_dtype == LR_BF16 ? EPI_STORE_BF16 : EPI_STORE_F32, y, ldy);
+  st = run_ops(M, &down, 1, dev_status, cs);
+  if (st != LR_OK) return st;
+  return run_ops(M, &up, 1, dev_status, cs);
+}
+
+size_t lr_block_scratch_bytes(int64_t M, const lr_block_desc* b) {
+  if (b == nullptr || M < 0) return 0;
+  return block_layout(M, b).total;
+}
+
+lr_status lr_block_forward(float* h, int64_t M, const lr_block_desc* b, void* scratch,
+                           size_t scratch_bytes, int32_t* dev_status, lr_stream s) {
+  lr_status st = check_block(b);
+  if (st != LR_OK) return st;
+  if (M < 0 || M > (int64_t(1) << 31) - 1) return invalid("block: bad M");
+  if (M == 0) return LR_OK;
+  if (h == nullptr || scratch == nullptr) return invalid("block: null pointer");
+  if (!aligned16(h) || reinterpret_cast<uintptr_t>(scratch) % kAlign)
+    return invalid("block: h must be 16-byte and scratch 256-byte aligned");
+  if (scratch_bytes < lr_block_scratch_bytes(M, b)) return invalid("block: scratch too small");
+  return enqueue_block(h, M, b, static_cast<uint8_t*>(scratch), dev_status,
+                       reinterpret_cast<cudaStream_t>(s));
+}
+
+lr_status remap_compact(const void* pool, int64_t pool_rows, int64_t row_bytes,
+                        const int32_t* remap, const int32_t* n_active, void* buf, int64_t cap,
+                        int32_t* dev_status, lr_stream s) {
+  if (cap < 0 || pool_rows < 0) return invalid("remap_compact: negative size");
+  if (row_bytes <= 0 || row_bytes % 16) return invalid("remap_compact: row_bytes must be a positive multiple of 16");
+  if (cap == 0) return LR_OK;
+  if (!pool || !remap || !n_active || !buf) return invalid("remap_compact: null pointer");
+  if (!aligned16(pool) || !aligned16(buf)) return invalid("remap_compact: misaligned buffer");
+  if (cap > 0x7FFFFFFF) return invalid("remap_compact: cap too large");
+  return launch_gather(pool, pool_rows, row_bytes, remap, n_active, buf, cap, dev_status,
+                       reinterpret_cast<cudaStream_t>(s));
+}
+
+lr_status remap_scatter(const void* buf, const int32_t* remap, const int32_t* n_active,
+                        void* pool, int64_t pool_rows, int64_t row_bytes, int64_t cap,
+                        int32_t* dev_status, lr_stream s) {
+  if (cap < 0 || pool_rows < 0) return invalid("remap_scatter: negative size");
+  if (row_bytes <= 0 || row_bytes % 16) return invalid("remap_scatter: row_bytes must be a positive multiple of 16");
+  if (cap == 0) return LR_OK;
+  if (!pool || !remap || !n_active || !buf) return invalid("remap_scatter: null pointer");
+  if (!aligned16(pool) || !aligned16(buf)) return invalid("remap_scatter: misaligned buffer");
+  if (cap > 0x7FFFFFFF) return invalid("remap_scatter: cap too large");
+  return launch_scatter(buf, remap, n_active, pool, pool_rows, row_bytes, cap, dev_status,
+                        reinterpret_cast<cudaStream_t>(s));
+}
+
+lr_status remap_build(const int32_t* lengths, int64_t n_seq, const int32_t* block_table,
+                      int32_t blocks_per_seq, int32_t block_rows, int32_t tail_rows, int64_t cap,
+                      int32_t* remap_out, int32_t* n_active_out, int32_t* n_runs_out) {
+  if (n_seq < 0 || cap < 0 || block_rows <= 0 || blocks_per_seq < 0)
+    return invalid("remap_build: bad sizes");
+  if ((n_seq > 0 && (!lengths || !block_table)) || (cap > 0 && !remap_out) || !n_active_out ||
+      !n_runs_out)
+    return invalid("remap_build: null pointer");
+  int64_t n = 0;
+  for (int64_t s = 0; s < n_seq; ++s) {
+    const int64_t L = lengths[s];
+    if (L < 0 || L > static_cast<int64_t>(blocks_per_seq) * block_rows)
+      return invalid("remap_build: length %lld of sequence %lld does not fit its table row",
+                     (long long)L, (long long)s);
+    const int64_t start = tail_rows <= 0 ? 0 : std::max<int64_t>(0, L - tail_rows);
+    for (int64_t p = start; p < L; ++p) {
+      const int32_t blk = block_table[s * blocks_per_seq + p / block_rows];
+      if (blk < 0) return invalid("remap_build: missing block for sequence %lld", (long long)s);
+      if (n >= cap) return invalid("remap_build: rows exceed cap %lld", (long long)cap);
+      const int64_t row = static_cast<int64_t>(blk) * block_rows + p % block_rows;
+      if (row > 0x7FFFFFFF) return invalid("remap_build: row index overflows int32");
+      remap_out[n++] = static_cast<int32_t>(row);
+    }
+  }
+  // Distinct targets: the scatter writes each pool row at most once.
+  std::vector<int32_t> sorted(remap_out, remap_out + n);
+  std::sort(sorted.begin(), sorted.end());
+  if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
+    return invalid("remap_build: two rows map to the same physical row");
+  int32_t runs = 0;
+  for (int64_t i = 0; i < n; ++i)
+    if (i == 0 || remap_out[i] != remap_out[i - 1] + 1) ++runs;
+  for (int64_t i = n; i < cap; ++i) remap_out[i] = -1;
+  *n_active_out = static_cast<int32_t>(n);
+  *n_runs_out = runs;
+  return LR_OK;
+}
+
+lr_status lr_stack_forward(const lr_stack_desc* st, lr_stream s) {
+  lr_status r = check_stack(st);
+  if (r != LR_OK) return r;
+  return enqueue_stack(st, reinterpret_cast<cudaStream_t>(s));
+}
+
+int64_t lr_stack_launch_count(const lr_stack_desc* st) {
+  if (st == nullptr || st->layers == nullptr) return 0;
+  int64_t n = 4;  // gather, widen, narrow, scatter
+  for (int l = 0; l < st->n_layers; ++l) n += block_launches(st->cap, &st->layers[l]);
+  return n;
+}
+
+lr_status lr_graph_capture(const lr_stack_desc* st, lr_graph** out) {
+  if (out == nullptr) return invalid("graph_capture: null output");
+  *out = nullptr;
+  lr_status r = check_stack(st);
+  if (r != LR_OK) return r;
+  r = ensure_configured();
+  if (r != LR_OK) return r;
+  cudaStream_t cs = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_fail(e, "graph_capture: stream");
+  lr_graph* g = new lr_graph();
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) {
+    r = cuda_fail(e, "graph_capture: begin");
+  } else {
+    lr_status r2 = enqueue_stack(st, cs);
+    e = cudaStreamEndCapture(cs, &g->graph);
+    if (r2 != LR_OK) r = r2;
+    else if (e != cudaSuccess) r = cuda_fail(e, "graph_capture: end");
+    else {
+      e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+      if (e != cudaSuccess) r = cuda_fail(e, "graph_capture: instantiate");
+    }
+  }
+  cudaStreamDestroy(cs);
+  if (r != LR_OK) {
+    if (g->exec) cudaGraphExecDestroy(g->exec);
+    if (g->graph) cudaGraphDestroy(g->graph);
+    delete g;
+    return r;
+  }
+  *out = g;
+  return LR_OK;
+}
+
+lr_status lr_graph_replay(lr_graph* g, lr_stream s) {
+  if (g == nullptr || g->magic != 0x4C524750u || g->exec == nullptr) {
+    set_error("graph_replay: not a live graph");
+    return LR_ERR_STATE;
+  }
+  cudaError_t e = cudaGraphLaunch(g->exec, reinterpret_cast<cudaStream_t>(s));
+  if (e != cudaSuccess) return cuda_fail(e, "graph_replay");
+  return LR_OK;
+}
+
+lr_status lr_graph_destroy(lr_graph* g) {
+  if (g == nullptr || g->magic != 0x4C524750u) {
+    set_error("graph_destroy: not a live graph");
+    return LR_ERR_STATE;
+  }
+  g->magic = 0;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
+  return LR_OK;
+}
+
+}  // extern "C"

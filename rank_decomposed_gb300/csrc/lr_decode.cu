@@ -1,0 +1,378 @@
+// Decode-size GEMMs (M <= 256 rows): out[m][n] = sum_k act[m][k] * W[n][k].
+//
+// These are the down and up projections of a decomposed layer (DeInfer, English
+// summary page section 2.A) at decode batch sizes, where the time is the
+// stream of factor bytes from HBM.  Design for sm_103a:
+//  * swap-AB on the 5th-generation tensor cores: a 128-row tile of the weight
+//    is the MMA's M side and the (padded) tokens are its N side, so M = 1..256
+//    tokens all run on tcgen05 with an fp32 accumulator in TMEM;
+//  * weight and activation tiles arrive by TMA (128-byte swizzle) through a
+//    multi-stage mbarrier ring; one thread issues the MMAs;
+//  * the K dimension of each 128-row tile is split over the CTAs of one
+//    thread-block cluster; their fp32 partial tiles are summed in a fixed
+//    order through distributed shared memory, so no workspace, no counters
+//    and no floating-point atomics are involved and the result is
+//    deterministic;
+//  * up to three problems with the same input (q/k/v, gate/up) share one
+//    launch;
+//  * programmatic dependent launch: weight tiles (which never depend on the
+//    previous kernel) are requested before griddepcontrol.wait, activation
+//    tiles after it.
+#include <cuda_bf16.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "lr_ptx.cuh"
+
+namespace lr {
+namespace {
+
+constexpr int kThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
+constexpr int kTileN = 128;    // weight rows per tile = MMA M
+constexpr int kBK = 64;        // reduction depth of one pipeline stage
+constexpr int kWBytes = kTileN * kBK * 2;
+
+template <int NT>
+struct DecodeCfg;
+template <> struct DecodeCfg<16> { static constexpr int kStages = 6; static constexpr int kSlots = 2; };
+template <> struct DecodeCfg<32> { static constexpr int kStages = 5; static constexpr int kSlots = 2; };
+template <> struct DecodeCfg<64> { static constexpr int kStages = 4; static constexpr int kSlots = 2; };
+template <> struct DecodeCfg<128> { static constexpr int kStages = 3; static constexpr int kSlots = 2; };
+template <> struct DecodeCfg<256> { static constexpr int kStages = 4; static constexpr int kSlots = 1; };
+
+template <int NT>
+constexpr int decode_smem_bytes() {
+  return DecodeCfg<NT>::kStages * (kWBytes + NT * kBK * 2) + 1024;
+}
+
+__device__ __forceinline__ int act_col(const DecodeProblem& P, int kb) {
+  const int k = kb * kBK;
+  if (P.gqa_head_dim > 0) {
+    const int head = k / P.gqa_head_dim;
+    return (head / P.gqa_group) * P.gqa_head_dim + (k % P.gqa_head_dim);
+  }
+  return k;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void store_out(const DecodeProblem& P, int m, int n, float v) {
+  const int64_t off = static_cast<int64_t>(m) * P.ldo + n;
+  if (P.epi == EPI_STORE_BF16) {
+    static_cast<uint16_t*>(P.out)[off] = f32_to_bf16_rn(v);
+  } else if (P.epi == EPI_STORE_F32) {
+    static_cast<float*>(P.out)[off] = v;
+  } else {
+    float* o = static_cast<float*>(P.out) + off;
+    *o = *o + v;
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ DecodeMaps maps) {
+  constexpr int kStages = DecodeCfg<NT>::kStages;
+  constexpr int kABytes = NT * kBK * 2;
+  constexpr uint32_t kStageBytes = kWBytes + kABytes;
+  constexpr uint32_t kTmemCols = NT < 32 ? 32 : NT;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kTileN, NT);
+
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ __align__(8) uint64_t accum_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  extern __shared__ uint8_t dyn_smem[];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.splits;
+  const int item = blockIdx.x;
+  int g = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxGroup; ++i)
+    if (i < p.n_problems && item >= p.prob[i].item_begin) g = i;
+  const DecodeProblem& P = p.prob[g];
+  const int local = item - P.item_begin;
+  const int tile = local / S;
+  const int split = local % S;  // == rank inside the cluster
+  const int kb0 = split * P.nkb / S;
+  const int nk = (split + 1) * P.nkb / S - kb0;
+  const int n0 = tile * kTileN;
+
+  const uint32_t raw = smem_u32(dyn_smem);
+  uint8_t* smem = dyn_smem + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t* w_smem = smem;
+  uint8_t* a_smem = smem + kStages * kWBytes;
+  float* ptile = reinterpret_cast<float*>(smem);  // [NT][128] once the MMAs are done
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&accum_bar, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const CUtensorMap* mw = &maps.w[g];
+      const CUtensorMap* ma = &maps.a[g];
+      prefetch_tensormap(mw);
+      prefetch_tensormap(ma);
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_a = l2_policy_evict_last();
+      const int npre = nk < kStages ? nk : kStages;
+      // Weight tiles do not depend on earlier kernels: request them first.
+      for (int i = 0; i < npre; ++i) {
+        mbar_arrive_expect_tx(&full_bar[i], kStageBytes);
+        tma_load_2d(w_smem + i * kWBytes, mw, &full_bar[i], (kb0 + i) * kBK, n0, pol_w);
+      }
+      pdl_wait();
+      for (int i = 0; i < npre; ++i)
+        tma_load_2d(a_smem + i * kABytes, ma, &full_bar[i], act_col(P, kb0 + i), 0, pol_a);
+      int issued = npre;
+      for (int i = npre; i < nk; ++i) {
+        const int s = i % kStages;
+        if (!mbar_wait(&empty_bar[s], ((i / kStages) - 1) & 1, &abort_sh)) {
+          abort_sh = 1;
+          report_status(p.status, LR_ERR_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
+        tma_load_2d(w_smem + s * kWBytes, mw, &full_bar[s], (kb0 + i) * kBK, n0, pol_w);
+        tma_load_2d(a_smem + s * kABytes, ma, &full_bar[s], act_col(P, kb0 + i), 0, pol_a);
+        ++issued;
+      }
+      if (abort_sh) {
+        // Let the copies already issued land before the CTA can exit.
+        for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+          mbar_wait(&full_bar[i % kStages], (i / kStages) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % kStages;
+        if (!mbar_wait(&full_bar[s], (i / kStages) & 1, &abort_sh)) {
+          abort_sh = 1;
+          report_status(p.status, LR_ERR_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = smem_desc_sw128(smem_u32(w_smem + s * kWBytes));
+        const uint64_t bd = smem_desc_sw128(smem_u32(a_smem + s * kABytes));
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k)
+          tc_mma_bf16(tmem, ad + 2 * k, bd + 2 * k, kIdesc, (i | k) != 0 ? 1u : 0u);
+        tc_commit(&empty_bar[s]);
+      }
+      tc_commit(&accum_bar);
+      // Every MMA issued by this thread completes before TMEM is released.
+      mbar_wait(&accum_bar, 0, nullptr);
+    }
+  } else {
+    // Epilogue warps: TMEM lanes 32*(warp%4) .. +31 hold weight rows; the
+    // columns are tokens.  Copy the valid tokens into this CTA's partial tile.
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    bool ok = mbar_wait(&accum_bar, 0, &abort_sh);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < NT / 16; ++c) {
+        if (c * 16 >= p.M) break;
+        uint32_t r[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = c * 16 + j;
+          if (tok < p.M) ptile[tok * kTileN + row] = __uint_as_float(r[j]);
+        }
+      }
+    } else if (lane == 0) {
+      abort_sh = 1;
+      report_status(p.status, LR_ERR_TIMEOUT);
+    }
+  }
+
+  __syncwarp();
+  cluster_sync_all();  // every partial tile of the cluster is in shared memory
+
+  if (warp >= 2) {
+    pdl_wait();  // outputs (e.g. the residual stream) belong to earlier kernels
+    const int row = (warp & 3) * 32 + lane;
+    const int n = n0 + row;
+    const int t0 = split * p.M / S;
+    const int t1 = (split + 1) * p.M / S;
+    if (n < P.N) {
+      for (int tok = t0; tok < t1; ++tok) {
+        const float* src = ptile + tok * kTileN + row;
+        float acc = 0.f;
+        for (int s2 = 0; s2 < S; ++s2) acc += ld_cluster_f32(src, static_cast<uint32_t>(s2));
+        store_out(P, tok, n, acc);
+      }
+    }
+  }
+
+  __syncwarp();
+  cluster_sync_all();  // no CTA leaves while others read its shared memory
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  return (v && *v) ? atoi(v) : dflt;
+}
+
+// Pick the number of K splits (= cluster size) of a launch: minimise the
+// per-SM share of weight tiles plus a per-wave overhead, in units of one
+// 128 x 64 weight tile.
+int choose_splits(const GemmOp* ops, int n_ops, int slots) {
+  static const int forced = env_int("LR_DECODE_SPLITS", 0);
+  int tiles = 0, min_nkb = 1 << 30;
+  for (int g = 0; g < n_ops; ++g) {
+    tiles += (ops[g].N + kTileN - 1) / kTileN;
+    min_nkb = std::min(min_nkb, ops[g].K / kBK);
+  }
+  const int smax = std::min(kMaxCluster, min_nkb);
+  if (forced > 0) return std::min(forced, smax);
+  const int sms = num_sms();
+  const double overhead = 4.0;
+  int best = 1;
+  double best_cost = 1e30;
+  for (int S = 1; S <= smax; ++S) {
+    const long C = static_cast<long>(tiles) * S;
+    int umax = 0;
+    for (int g = 0; g < n_ops; ++g) umax = std::max(umax, (ops[g].K / kBK + S - 1) / S);
+    const double per_sm = std::ceil(static_cast<double>(C) / sms) * umax;
+    const double waves = std::ceil(static_cast<double>(C) / (static_cast<double>(sms) * slots));
+    const double cost = per_sm + overhead * waves;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
+}
+
+template <int NT>
+lr_status configure_nt() {
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       decode_smem_bytes<NT>());
+  if (e != cudaSuccess) return cuda_fail(e, "decode: set smem");
+  e = cudaFuncSetAttribute(decode_kernel<NT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return cuda_fail(e, "decode: allow clusters of 16");
+  return LR_OK;
+}
+
+template <int NT>
+lr_status launch_nt(int M, const GemmOp* ops, int n_ops, int32_t* status, cudaStream_t s) {
+  constexpr int kSmem = decode_smem_bytes<NT>();
+  DecodeParams prm;
+  memset(&prm, 0, sizeof(prm));
+  DecodeMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  prm.M = M;
+  prm.n_problems = n_ops;
+  prm.status = status;
+  const int S = choose_splits(ops, n_ops, DecodeCfg<NT>::kSlots);
+  prm.splits = S;
+  int items = 0;
+  for (int g = 0; g < n_ops; ++g) {
+    const GemmOp& o = ops[g];
+    lr_status st = encode_map_bf16(&maps.w[g], o.W, o.N, o.K, o.ldw, kTileN);
+    if (st != LR_OK) return st;
+    st = encode_map_bf16(&maps.a[g], o.act, M, o.act_cols, o.ld_act, NT);
+    if (st != LR_OK) return st;
+    DecodeProblem& P = prm.prob[g];
+    P.N = o.N;
+    P.nkb = o.K / kBK;
+    P.n_tiles = (o.N + kTileN - 1) / kTileN;
+    P.item_begin = items;
+    P.gqa_head_dim = o.gqa_head_dim;
+    P.gqa_group = o.gqa_group;
+    P.epi = o.epi;
+    P.out = o.out;
+    P.ldo = o.ldo;
+    items += P.n_tiles * S;
+  }
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(items, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = S;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<NT>, prm, maps);
+  if (e != cudaSuccess) return cuda_fail(e, "decode: launch");
+  return LR_OK;
+}
+
+}  // namespace
+
+lr_status configure_decode() {
+  lr_status st;
+  if ((st = configure_nt<16>()) != LR_OK) return st;
+  if ((st = configure_nt<32>()) != LR_OK) return st;
+  if ((st = configure_nt<64>()) != LR_OK) return st;
+  if ((st = configure_nt<128>()) != LR_OK) return st;
+  return configure_nt<256>();
+}
+
+lr_status launch_decode(int M, const GemmOp* ops, int n_ops, int32_t* status, cudaStream_t s) {
+  if (M <= 16) return launch_nt<16>(M, ops, n_ops, status, s);
+  if (M <= 32) return launch_nt<32>(M, ops, n_ops, status, s);
+  if (M <= 64) return launch_nt<64>(M, ops, n_ops, status, s);
+  if (M <= 128) return launch_nt<128>(M, ops, n_ops, status, s);
+  return launch_nt<256>(M, ops, n_ops, status, s);
+}
+
+}  // namespace lr

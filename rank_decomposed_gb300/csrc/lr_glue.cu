@@ -1,0 +1,245 @@
+// Memory-bound kernels around the GEMMs: the remap gather/scatter of the
+// preparation and graph-replay stages (DeInfer, English summary page section
+// 2.C), RMSNorm, SiLU-GLU and the bf16 <-> fp32 conversions of the residual
+// stream.  All use 16-byte vector accesses; reductions run in a fixed order so
+// every result is deterministic.
+#include <cuda_bf16.h>
+
+#include <cstring>
+
+#include "lr_ptx.cuh"
+
+namespace lr {
+namespace {
+
+// Launch with programmatic dependent launch when enabled; every kernel here
+// calls pdl_wait() before it touches memory written by earlier kernels.
+template <typename... KArgs, typename... Args>
+lr_status launch(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t s, const char* what,
+                 Args... args) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (pdl_enabled()) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return LR_OK;
+}
+
+__device__ __forceinline__ int clamp_active(const int32_t* n_active, int64_t cap) {
+  int n = *n_active;
+  if (n < 0) n = 0;
+  if (n > cap) n = static_cast<int>(cap);
+  return n;
+}
+
+// buf[i] = pool[remap[i]] for i < n_active, zero rows otherwise.
+__global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ pool, int64_t pool_rows,
+                                                     int64_t row_vecs, const int32_t* __restrict__ remap,
+                                                     const int32_t* __restrict__ n_active,
+                                                     uint4* __restrict__ buf, int64_t cap,
+                                                     int32_t* status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t i = blockIdx.x;
+  const int n = clamp_active(n_active, cap);
+  uint4* dst = buf + i * row_vecs;
+  const uint4* src = nullptr;
+  if (i < n) {
+    const int64_t j = remap[i];
+    if (j >= 0 && j < pool_rows) {
+      src = pool + j * row_vecs;
+    } else if (threadIdx.x == 0) {
+      report_status(status, LR_ERR_REMAP_RANGE);
+    }
+  }
+  if (src != nullptr) {
+    for (int64_t v = threadIdx.x; v < row_vecs; v += blockDim.x) dst[v] = src[v];
+  } else {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int64_t v = threadIdx.x; v < row_vecs; v += blockDim.x) dst[v] = z;
+  }
+}
+
+// pool[remap[i]] = buf[i] for i < n_active.
+__global__ void __launch_bounds__(256) scatter_kernel(const uint4* __restrict__ buf,
+                                                      const int32_t* __restrict__ remap,
+                                                      const int32_t* __restrict__ n_active,
+                                                      uint4* __restrict__ pool, int64_t pool_rows,
+                                                      int64_t row_vecs, int64_t cap,
+                                                      int32_t* status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t i = blockIdx.x;
+  const int n = clamp_active(n_active, cap);
+  if (i >= n) return;
+  const int64_t j = remap[i];
+  if (j < 0 || j >= pool_rows) {
+    if (threadIdx.x == 0) report_status(status, LR_ERR_REMAP_RANGE);
+    return;
+  }
+  const uint4* src = buf + i * row_vecs;
+  uint4* dst = pool + j * row_vecs;
+  for (int64_t v = threadIdx.x; v < row_vecs; v += blockDim.x) dst[v] = src[v];
+}
+
+// out[m] = bf16(h[m] / sqrt(mean(h[m]^2) + eps)); one CTA per row.
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float4* __restrict__ h,
+                                                      uint2* __restrict__ out, int d4, float eps) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ float part[8];
+  const int64_t row = blockIdx.x;
+  const float4* x = h + row * d4;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d4; i += blockDim.x) {
+    const float4 v = x[i];
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += part[w];
+  const float inv = 1.0f / sqrtf(tot / static_cast<float>(4 * d4) + eps);
+  uint2* y = out + row * d4;
+  for (int i = threadIdx.x; i < d4; i += blockDim.x) {
+    const float4 v = x[i];
+    uint2 w;
+    w.x = static_cast<uint32_t>(f32_to_bf16_rn(v.x * inv)) |
+          (static_cast<uint32_t>(f32_to_bf16_rn(v.y * inv)) << 16);
+    w.y = static_cast<uint32_t>(f32_to_bf16_rn(v.z * inv)) |
+          (static_cast<uint32_t>(f32_to_bf16_rn(v.w * inv)) << 16);
+    y[i] = w;
+  }
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// a = bf16(silu(g) * u), 8 elements per vector.
+__global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__ g,
+                                                       const uint4* __restrict__ u,
+                                                       uint4* __restrict__ a, int64_t n8) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 gv = g[i];
+    const uint4 uv = u[i];
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+    uint32_t ow[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float g0 = bf16_to_f32(static_cast<uint16_t>(gw[j] & 0xFFFFu));
+      const float g1 = bf16_to_f32(static_cast<uint16_t>(gw[j] >> 16));
+      const float u0 = bf16_to_f32(static_cast<uint16_t>(uw[j] & 0xFFFFu));
+      const float u1 = bf16_to_f32(static_cast<uint16_t>(uw[j] >> 16));
+      ow[j] = static_cast<uint32_t>(f32_to_bf16_rn(silu_f(g0) * u0)) |
+              (static_cast<uint32_t>(f32_to_bf16_rn(silu_f(g1) * u1)) << 16);
+    }
+    a[i] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+  }
+}
+
+__global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ in,
+                                                    float4* __restrict__ out, int64_t n8) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = in[i];
+    out[2 * i] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                             __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+    out[2 * i + 1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u),
+                                 __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+  }
+}
+
+__global__ void __launch_bounds__(256) narrow_kernel(const float4* __restrict__ in,
+                                                     uint4* __restrict__ out, int64_t n8) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = in[2 * i];
+    const float4 b = in[2 * i + 1];
+    uint4 w;
+    w.x = static_cast<uint32_t>(f32_to_bf16_rn(a.x)) | (static_cast<uint32_t>(f32_to_bf16_rn(a.y)) << 16);
+    w.y = static_cast<uint32_t>(f32_to_bf16_rn(a.z)) | (static_cast<uint32_t>(f32_to_bf16_rn(a.w)) << 16);
+    w.z = static_cast<uint32_t>(f32_to_bf16_rn(b.x)) | (static_cast<uint32_t>(f32_to_bf16_rn(b.y)) << 16);
+    w.w = static_cast<uint32_t>(f32_to_bf16_rn(b.z)) | (static_cast<uint32_t>(f32_to_bf16_rn(b.w)) << 16);
+    out[i] = w;
+  }
+}
+
+int elementwise_grid(int64_t n_vec) {
+  const int64_t per = 256;
+  int64_t blocks = (n_vec + per - 1) / per;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+lr_status launch_gather(const void* pool, int64_t pool_rows, int64_t row_bytes,
+                        const int32_t* remap, const int32_t* n_active, void* buf, int64_t cap,
+                        int32_t* status, cudaStream_t s) {
+  if (cap == 0) return LR_OK;
+  return launch(gather_kernel, dim3(static_cast<unsigned>(cap)), dim3(256), s, "gather",
+                static_cast<const uint4*>(pool), pool_rows, row_bytes / 16, remap, n_active,
+                static_cast<uint4*>(buf), cap, status);
+}
+
+lr_status launch_scatter(const void* buf, const int32_t* remap, const int32_t* n_active,
+                         void* pool, int64_t pool_rows, int64_t row_bytes, int64_t cap,
+                         int32_t* status, cudaStream_t s) {
+  if (cap == 0) return LR_OK;
+  return launch(scatter_kernel, dim3(static_cast<unsigned>(cap)), dim3(256), s, "scatter",
+                static_cast<const uint4*>(buf), remap, n_active, static_cast<uint4*>(pool),
+                pool_rows, row_bytes / 16, cap, status);
+}
+
+lr_status launch_rmsnorm(const float* h, void* out_bf16, int64_t M, int d, float eps,
+                         cudaStream_t s) {
+  if (M == 0) return LR_OK;
+  return launch(rmsnorm_kernel, dim3(static_cast<unsigned>(M)), dim3(256), s, "rmsnorm",
+                reinterpret_cast<const float4*>(h), static_cast<uint2*>(out_bf16), d / 4, eps);
+}
+
+lr_status launch_silu_mul(const void* g, const void* u, void* out, int64_t M, int d,
+                          cudaStream_t s) {
+  const int64_t n8 = M * d / 8;
+  if (n8 == 0) return LR_OK;
+  return launch(silu_mul_kernel, dim3(elementwise_grid(n8)), dim3(256), s, "silu_mul",
+                static_cast<const uint4*>(g), static_cast<const uint4*>(u),
+                static_cast<uint4*>(out), n8);
+}
+
+lr_status launch_widen(const void* in_bf16, float* out, int64_t n, cudaStream_t s) {
+  const int64_t n8 = n / 8;
+  if (n8 == 0) return LR_OK;
+  return launch(widen_kernel, dim3(elementwise_grid(n8)), dim3(256), s, "widen",
+                static_cast<const uint4*>(in_bf16), reinterpret_cast<float4*>(out), n8);
+}
+
+lr_status launch_narrow(const float* in, void* out_bf16, int64_t n, cudaStream_t s) {
+  const int64_t n8 = n / 8;
+  if (n8 == 0) return LR_OK;
+  return launch(narrow_kernel, dim3(elementwise_grid(n8)), dim3(256), s, "narrow",
+                reinterpret_cast<const float4*>(in), static_cast<uint4*>(out_bf16), n8);
+}
+
+}  // namespace lr

@@ -1,0 +1,125 @@
+// Internal declarations shared by the translation units of liblr.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/lr.h"
+
+namespace lr {
+
+// Every bounded wait inside a kernel gives up after this long.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Largest number of problems one grouped decode launch carries.
+constexpr int kMaxGroup = 3;
+
+// Decode (swap-AB) kernels take at most this many rows.
+constexpr int kDecodeMaxRows = 256;
+
+// Largest cluster used for the split-K reduction of the decode kernel.
+constexpr int kMaxCluster = 16;
+
+// What a GEMM does with each finished fp32 output element v at (m, n).
+enum Epilogue : int32_t {
+  EPI_STORE_BF16 = 0,  // out_bf16[m*ldo + n] = rne(v)
+  EPI_STORE_F32 = 1,   // out_f32[m*ldo + n] = v
+  EPI_ADD_F32 = 2,     // out_f32[m*ldo + n] += v   (residual stream)
+};
+
+// One problem of a GEMM launch:  out[m][n] = sum_k act[m][k] * W[n][k]
+// for m < M, n < N, k < K (K a multiple of 64).  W and act are bf16.
+struct GemmOp {
+  const void* W;        // [N][ldw]
+  int32_t N;
+  int32_t K;
+  int64_t ldw;
+  const void* act;      // [M][ld_act]
+  int64_t ld_act;
+  int64_t act_cols;     // columns of the act buffer (differs from K under GQA)
+  int32_t gqa_head_dim; // 0: act column = k.  Otherwise the act buffer holds
+  int32_t gqa_group;    //   kv heads and column k reads kv head (k/hd)/group.
+  int32_t epi;
+  void* out;
+  int64_t ldo;
+};
+
+// --------------------------------------------------- device-side parameters
+struct DecodeProblem {
+  int32_t N;
+  int32_t nkb;          // K / 64
+  int32_t n_tiles;      // ceil(N / 128)
+  int32_t item_begin;   // first CTA index of this problem
+  int32_t gqa_head_dim;
+  int32_t gqa_group;
+  int32_t epi;
+  int32_t pad_;
+  void* out;
+  int64_t ldo;
+};
+
+struct DecodeParams {
+  int32_t M;            // valid rows (tokens), 1..256
+  int32_t n_problems;
+  int32_t splits;       // K splits per tile == cluster size
+  int32_t pad_;
+  int32_t* status;
+  DecodeProblem prob[kMaxGroup];
+};
+
+struct DecodeMaps {
+  CUtensorMap w[kMaxGroup];
+  CUtensorMap a[kMaxGroup];
+};
+
+struct PrefillParams {
+  int32_t M, N, K;
+  int32_t m_tiles, n_tiles;
+  int32_t epi;
+  int32_t gqa_head_dim, gqa_group;
+  void* out;
+  int64_t ldo;
+  int32_t* status;
+};
+
+// ------------------------------------------------------------- host helpers
+void set_error(const char* fmt, ...);
+lr_status cuda_fail(cudaError_t e, const char* what);
+
+// Tensor map over a bf16 row-major [rows][cols] matrix with row stride ld
+// (elements), box = box_rows x 64 columns, 128-byte swizzle, zero fill
+// outside the matrix.
+lr_status encode_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                          uint64_t ld, uint32_t box_rows);
+
+int num_sms();
+
+// Launchers (lr_decode.cu, lr_prefill.cu, lr_glue.cu).  They assume their
+// arguments were validated by the caller.
+lr_status launch_decode(int M, const GemmOp* ops, int n_ops, int32_t* status, cudaStream_t s);
+lr_status launch_prefill(int64_t M, const GemmOp& op, int32_t* status, cudaStream_t s);
+lr_status launch_rmsnorm(const float* h, void* out_bf16, int64_t M, int d, float eps,
+                         cudaStream_t s);
+lr_status launch_silu_mul(const void* g, const void* u, void* out, int64_t M, int d,
+                          cudaStream_t s);
+lr_status launch_widen(const void* in_bf16, float* out, int64_t n, cudaStream_t s);
+lr_status launch_narrow(const float* in, void* out_bf16, int64_t n, cudaStream_t s);
+lr_status launch_gather(const void* pool, int64_t pool_rows, int64_t row_bytes,
+                        const int32_t* remap, const int32_t* n_active, void* buf, int64_t cap,
+                        int32_t* status, cudaStream_t s);
+lr_status launch_scatter(const void* buf, const int32_t* remap, const int32_t* n_active,
+                         void* pool, int64_t pool_rows, int64_t row_bytes, int64_t cap,
+                         int32_t* status, cudaStream_t s);
+
+// Kernel attributes (dynamic shared memory, cluster size) of the current
+// device; done once per device before the first launch or capture.
+lr_status configure_decode();
+lr_status configure_prefill();
+lr_status ensure_configured();
+
+// Launch attribute helper: programmatic dependent launch on/off for kernels
+// enqueued by this library (on by default).
+bool pdl_enabled();
+
+}  // namespace lr

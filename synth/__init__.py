@@ -129,9 +129,29 @@ def f64_to_bf16_bits(v: np.ndarray) -> np.ndarray:
     return out.astype(np.uint16)
 
 
-def bf16_normal(seed: int, tag: int, shape, std: float = 1.0,
-                col_scale: np.ndarray | None = None) -> np.ndarray:
-    """bf16 bit patterns (uint16, row-major ``shape``) of ``z * std [* col_scale]``."""
+_host_lib = None
+
+
+def _host():
+    """The C implementation (synth_host.c), or None when it has not been built."""
+    global _host_lib
+    if _host_lib is None:
+        import ctypes
+        import os
+        path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsynth_host.so")
+        if not os.path.exists(path):
+            return None
+        lib = ctypes.CDLL(path)
+        lib.synth_bf16_normal_host.restype = ctypes.c_int
+        lib.synth_bf16_normal_host.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                               ctypes.c_uint64, ctypes.c_double, ctypes.c_void_p]
+        _host_lib = lib
+    return _host_lib
+
+
+def bf16_normal_numpy(seed: int, tag: int, shape, std: float = 1.0,
+                      col_scale: np.ndarray | None = None) -> np.ndarray:
+    """The definition in numpy (slow; the reference for the C and CUDA versions)."""
     shape = tuple(int(s) for s in shape)
     n = int(np.prod(shape)) if shape else 1
     v = normal_f64(stream_key(seed, tag), n) * np.float64(std)
@@ -141,6 +161,28 @@ def bf16_normal(seed: int, tag: int, shape, std: float = 1.0,
             raise ValueError("col_scale must have one entry per column")
         v = (v.reshape(-1, shape[-1]) * cs[None, :]).reshape(-1)
     return f64_to_bf16_bits(v).reshape(shape)
+
+
+def bf16_normal(seed: int, tag: int, shape, std: float = 1.0,
+                col_scale: np.ndarray | None = None) -> np.ndarray:
+    """bf16 bit patterns (uint16, row-major ``shape``) of ``z * std [* col_scale]``."""
+    lib = _host()
+    shape = tuple(int(s) for s in shape)
+    if lib is None or len(shape) == 0:
+        return bf16_normal_numpy(seed, tag, shape, std, col_scale)
+    rows = int(np.prod(shape[:-1])) if len(shape) > 1 else 1
+    cols = shape[-1]
+    out = np.empty(shape, dtype=np.uint16)
+    cs = None
+    if col_scale is not None:
+        cs = np.ascontiguousarray(col_scale, dtype=np.float64)
+        if cs.shape != (cols,):
+            raise ValueError("col_scale must have one entry per column")
+    bad = lib.synth_bf16_normal_host(out.ctypes.data, rows, cols, stream_key(seed, tag),
+                                     float(std), None if cs is None else cs.ctypes.data)
+    if bad:
+        raise ValueError("value outside the normal bf16 range")
+    return out
 
 
 def permutation(seed: int, tag: int, n: int) -> np.ndarray:
@@ -218,3 +260,32 @@ def paged_batch(seed: int, n_seq: int, len_lo: int, len_hi: int, block_rows: int
 def gpu_gen_lib_path() -> str:
     import os
     return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsynth.so")
+
+
+_gpu_lib = None
+
+
+def _gpu():
+    global _gpu_lib
+    if _gpu_lib is None:
+        import ctypes
+        lib = ctypes.CDLL(gpu_gen_lib_path())
+        lib.synth_bf16_normal.restype = ctypes.c_int
+        lib.synth_bf16_normal.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                          ctypes.c_uint64, ctypes.c_double, ctypes.c_void_p,
+                                          ctypes.c_void_p]
+        _gpu_lib = lib
+    return _gpu_lib
+
+
+def fill_bf16_normal_device(ptr: int, rows: int, cols: int, seed: int, tag: int,
+                            std: float = 1.0, col_scale_ptr: int | None = None,
+                            stream: int | None = None) -> None:
+    """Device version of ``bf16_normal``: writes ``rows x cols`` bf16 values at ``ptr``.
+
+    ``col_scale_ptr`` is a device array of ``cols`` fp64 scales (or None).
+    """
+    rc = _gpu().synth_bf16_normal(ptr, rows, cols, stream_key(seed, tag), float(std),
+                                  col_scale_ptr, stream)
+    if rc != 0:
+        raise RuntimeError("synth_bf16_normal failed with CUDA error %d" % rc)

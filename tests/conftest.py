@@ -10,3 +10,15 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+def _ensure_built():
+    lib = os.path.join(ROOT, "rank_decomposed_gb300", "liblr.so")
+    gen = os.path.join(ROOT, "synth", "libsynth.so")
+    host = os.path.join(ROOT, "synth", "libsynth_host.so")
+    if not (os.path.exists(lib) and os.path.exists(gen) and os.path.exists(host)):
+        from rank_decomposed_gb300 import build as _b
+        _b.build()
+
+
+_ensure_built()

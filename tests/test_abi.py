@@ -1,0 +1,156 @@
+"""The C-ABI library without a GPU: exports, host-side remap scan, argument checks."""
+
+import ctypes
+import json
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+import rank_decomposed_gb300 as lr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "lr.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s+\**([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_function():
+    names = header_functions()
+    assert "lr_linear_forward" in names and "remap_compact" in names and "lr_graph_replay" in names
+    assert len(names) >= 14
+    out = subprocess.run(["nm", "-D", "--defined-only", lr.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(l.split()[-1] for l in out.splitlines() if l.strip())
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+
+
+def test_status_strings():
+    assert lr.status_string(lr.LR_OK) == "ok"
+    assert "remap" in lr.status_string(lr.LR_ERR_REMAP_RANGE)
+    assert lr.status_string(99) == "unknown status"
+
+
+def test_remap_build_golden_and_oracle():
+    with open(os.path.join(GOLDEN, "remap_build_small.json")) as f:
+        g = json.load(f)
+    table = np.array(g["block_table"], dtype=np.int32)
+    for c in g["cases"]:
+        remap, na, nr = lr.remap_build(g["lengths"], table, g["block_rows"], c["tail_rows"], c["cap"])
+        assert remap.tolist() == c["remap"]
+        assert (na, nr) == (c["n_active"], c["n_runs"])
+
+
+@pytest.mark.parametrize("tail", [1, 3, 0])
+def test_remap_build_matches_oracle_on_paged_batch(tail):
+    L, table, total = synth.paged_batch(3, 24, 1, 200, 16)
+    cap = int(L.sum()) if tail == 0 else 24 * tail
+    got = lr.remap_build(L, table, 16, tail, cap)
+    want = oracle.remap_build(L, table, 16, tail, cap)
+    assert np.array_equal(got[0], want[0])
+    assert got[1:] == want[1:]
+
+
+def test_remap_build_errors():
+    L = np.array([5, 3], np.int32)
+    T = np.array([[0, 1], [2, -1]], np.int32)
+    with pytest.raises(lr.LrError) as e:
+        lr.remap_build(L, T, 4, 0, 7)          # 8 rows > cap 7
+    assert e.value.status == lr.LR_ERR_INVALID_ARG
+    with pytest.raises(lr.LrError):
+        lr.remap_build(np.array([9], np.int32), np.array([[0, 1]], np.int32), 4, 0, 16)  # too long
+    with pytest.raises(lr.LrError):
+        lr.remap_build(np.array([2, 2], np.int32), np.array([[0], [0]], np.int32), 4, 0, 8)  # same rows
+    with pytest.raises(lr.LrError):
+        lr.remap_build(np.array([6], np.int32), np.array([[0, -1]], np.int32), 4, 0, 8)  # missing block
+
+
+def _fake_factor(d_in, d_out, r, addr=0x10000):
+    return lr.Factor(addr, addr + 0x100000, d_in, d_out, r)
+
+
+def _linear(x, ldx, y, ldy, M, f, ws=0x300000, ws_bytes=1 << 30, ydt=lr.LR_F32):
+    return lr.lib.lr_linear_forward(x, ldx, y, ldy, ydt, M, ctypes.byref(f), ws, ws_bytes, None, None)
+
+
+def test_linear_argument_checks_launch_nothing():
+    good = _fake_factor(512, 512, 64)
+    assert _linear(0x1000, 512, 0x2000, 512, 0, good) == lr.LR_OK           # M = 0: no-op
+    assert _linear(0x1000, 512, 0x2000, 512, 4, _fake_factor(500, 512, 64)) == lr.LR_ERR_UNSUPPORTED
+    assert _linear(0x1000, 512, 0x2000, 512, 4, _fake_factor(512, 512, 100)) == lr.LR_ERR_UNSUPPORTED
+    assert _linear(None, 512, 0x2000, 512, 4, good) == lr.LR_ERR_INVALID_ARG
+    assert _linear(0x1008, 512, 0x2000, 512, 4, good) == lr.LR_ERR_INVALID_ARG  # x not 16-byte aligned
+    assert _linear(0x1000, 500, 0x2000, 512, 4, good) == lr.LR_ERR_INVALID_ARG  # ldx < d_in
+    assert _linear(0x1000, 512, 0x2000, 256, 4, good) == lr.LR_ERR_INVALID_ARG  # ldy < d_out
+    assert _linear(0x1000, 512, 0x2000, 512, 4, good, ws_bytes=16) == lr.LR_ERR_INVALID_ARG
+    assert _linear(0x1000, 512, 0x2000, 512, 4, good, ws=0x300010) == lr.LR_ERR_INVALID_ARG
+    assert _linear(0x1000, 512, 0x2000, 512, 4, good, ydt=7) == lr.LR_ERR_INVALID_ARG
+    assert _linear(0x1000, 512, 0x2000, 512, 4, lr.Factor(0x10008, 0x20000, 512, 512, 64)) == lr.LR_ERR_INVALID_ARG
+    assert "aligned" in lr.last_error()
+
+
+def test_workspace_sizes():
+    f = _fake_factor(4096, 4096, 1216)
+    assert lr.lib.lr_linear_workspace_bytes(64, ctypes.byref(f)) == 64 * 1216 * 2
+    assert lr.lib.lr_linear_workspace_bytes(3, ctypes.byref(f)) == 7424  # 3*1216*2 -> 256-aligned
+
+
+def _fake_block(d=512, dff=1024, nh=8, nkv=2, hd=64, ranks=(64, 64, 64, 64, 128, 128, 128)):
+    b = lr.BlockDesc()
+    b.d_model, b.d_ff, b.n_heads, b.n_kv_heads, b.head_dim, b.eps = d, dff, nh, nkv, hd, 1e-6
+    io = [(d, nh * hd), (d, nkv * hd), (d, nkv * hd), (nh * hd, d), (d, dff), (d, dff), (dff, d)]
+    for i, ((a, o), r) in enumerate(zip(io, ranks)):
+        b.f[i] = _fake_factor(a, o, r, 0x10000 * (i + 1))
+    return b
+
+
+def test_block_scratch_layout_matches_struct():
+    b = _fake_block()
+    M = 5
+    al = lambda x: (x + 255) // 256 * 256
+    want = al(M * 512 * 2) + sum(al(M * r * 2) for r in (64, 64, 64, 64, 128, 128, 128))
+    want += al(M * 512 * 2) + 2 * al(M * 128 * 2) + al(M * 512 * 2) + 3 * al(M * 1024 * 2)
+    assert lr.lib.lr_block_scratch_bytes(M, ctypes.byref(b)) == want
+
+
+def test_block_argument_checks():
+    b = _fake_block()
+    h, s = 0x100000, 0x200000
+    call = lambda bb, M=4, sb=1 << 30: lr.lib.lr_block_forward(h, M, ctypes.byref(bb), s, sb, None, None)
+    assert call(b, M=0) == lr.LR_OK
+    bad = _fake_block(nkv=3)
+    assert call(bad) == lr.LR_ERR_INVALID_ARG           # 8 heads not divisible by 3 kv heads
+    bad = _fake_block()
+    bad.f[1] = _fake_factor(512, 192, 64)               # k factor with the wrong output size
+    assert call(bad) == lr.LR_ERR_INVALID_ARG
+    assert call(_fake_block(hd=32, nh=16, nkv=4)) == lr.LR_ERR_UNSUPPORTED
+    assert call(b, sb=100) == lr.LR_ERR_INVALID_ARG
+
+
+def test_remap_copy_argument_checks():
+    f = lr.lib.remap_compact
+    assert f(0x1000, 10, 8192, 0x2000, 0x3000, 0x4000, 0, None, None) == lr.LR_OK   # cap 0
+    assert f(0x1000, 10, 100, 0x2000, 0x3000, 0x4000, 4, None, None) == lr.LR_ERR_INVALID_ARG
+    assert f(0x1008, 10, 8192, 0x2000, 0x3000, 0x4000, 4, None, None) == lr.LR_ERR_INVALID_ARG
+    assert f(0x1000, 10, 8192, None, 0x3000, 0x4000, 4, None, None) == lr.LR_ERR_INVALID_ARG
+    g = lr.lib.remap_scatter
+    assert g(0x4000, 0x2000, 0x3000, 0x1000, 10, 48, 0, None, None) == lr.LR_OK
+    assert g(0x4000, 0x2000, 0x3000, 0x1000, 10, 40, 4, None, None) == lr.LR_ERR_INVALID_ARG
+
+
+def test_graph_handles_checked():
+    assert lr.lib.lr_graph_replay(None, None) == lr.LR_ERR_STATE
+    assert lr.lib.lr_graph_destroy(None) == lr.LR_ERR_STATE
+    g = ctypes.c_void_p()
+    assert lr.lib.lr_graph_capture(None, ctypes.byref(g)) == lr.LR_ERR_INVALID_ARG

@@ -1,0 +1,137 @@
+"""GPU parity of the decomposed block and the graph-replayed layer stack."""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from lr_testutil import (assert_parity, block_shapes, dev_bits, dev_factor, host_bits, host_factor)
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+import rank_decomposed_gb300 as lr  # noqa: E402
+
+SMALL = dict(d=512, d_ff=1024, n_heads=8, n_kv=2, hd=64, ranks=(128, 64, 64, 128, 192, 192, 192))
+LLAMA7B = dict(d=4096, d_ff=11008, n_heads=32, n_kv=32, hd=128,
+               ranks=(1216, 1216, 1216, 1216, 1792, 1792, 1792))
+
+
+def make_layer(seed, layer, cfg):
+    shapes = block_shapes(cfg["d"], cfg["d_ff"], cfg["n_heads"], cfg["n_kv"], cfg["hd"], cfg["ranks"])
+    dev = [dev_factor(seed, layer, p, a, b, r) for p, (a, b, r) in enumerate(shapes)]
+    host = {synth.PROJ_NAMES[p]: host_factor(seed, layer, p, a, b, r)
+            for p, (a, b, r) in enumerate(shapes)}
+    blk = lr.Block(cfg["d"], cfg["d_ff"], cfg["n_heads"], cfg["n_kv"], cfg["hd"], dev)
+    return blk, host
+
+
+def _h_input(seed, M, d):
+    bits = synth.bf16_normal(seed, synth.make_tag(0, 0, synth.KIND_X), (M, d))
+    return bits, oracle.widen_bf16(bits)
+
+
+@pytest.mark.parametrize("M", [1, 4, 37, 300])
+def test_block_small_gqa(M):
+    cfg = SMALL
+    blk, host = make_layer(3, 0, cfg)
+    bits, h0 = _h_input(3, M, cfg["d"])
+    h = torch.from_numpy(h0.astype(np.float32)).cuda()
+    scratch = torch.zeros(lr.block_scratch_bytes(M, blk), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr.block_forward(h, blk, scratch, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = oracle.block_forward(h0, host, cfg["n_heads"], cfg["n_kv"], cfg["hd"])
+    out = h.cpu().numpy().astype(np.float64)
+    assert_parity(out - h0, ref - h0, "block delta M=%d" % M)
+    assert_parity(out, ref, "block M=%d" % M)
+
+
+def test_block_llama7b_decode64():
+    cfg = LLAMA7B
+    M = 64
+    blk, host = make_layer(0, 0, cfg)
+    bits, h0 = _h_input(0, M, cfg["d"])
+    h = torch.from_numpy(h0.astype(np.float32)).cuda()
+    scratch = torch.zeros(lr.block_scratch_bytes(M, blk), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr.block_forward(h, blk, scratch, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = oracle.block_forward(h0, host, cfg["n_heads"], cfg["n_kv"], cfg["hd"])
+    out = h.cpu().numpy().astype(np.float64)
+    assert_parity(out - h0, ref - h0, "7B block delta")
+
+
+def _make_stack(cfg, n_layers, cap, n_seq, seed=4):
+    layers, hosts = zip(*[make_layer(seed, l, cfg) for l in range(n_layers)])
+    L, table, total = synth.paged_batch(seed, n_seq, 20, 300, 16)
+    pool_rows = total * 16
+    pool_bits = synth.bf16_normal(seed, synth.make_tag(0, 0, synth.KIND_POOL), (pool_rows, cfg["d"]))
+    remap, n_active, _ = lr.remap_build(L, table, 16, 1, cap)
+    d = cfg["d"]
+    pool = dev_bits(pool_bits)
+    dev = dict(
+        pool_in=pool, pool_out=pool.clone(),
+        remap=torch.from_numpy(remap).cuda(),
+        n_active=torch.tensor([n_active], dtype=torch.int32, device="cuda"),
+        xbuf=torch.zeros(cap, d, dtype=torch.bfloat16, device="cuda"),
+        h=torch.zeros(cap, d, dtype=torch.float32, device="cuda"),
+        ybuf=torch.zeros(cap, d, dtype=torch.bfloat16, device="cuda"),
+        status=torch.zeros(1, dtype=torch.int32, device="cuda"))
+    dev["scratch"] = torch.zeros(lr.Stack.scratch_bytes(cap, layers), dtype=torch.uint8,
+                                 device="cuda")
+    stack = lr.Stack(list(layers), **dev)
+    return stack, list(hosts), pool_bits, remap, n_active
+
+
+def _oracle_stack(cfg, hosts, pool_bits, remap, n):
+    x = oracle.widen_bf16(pool_bits[remap[:n]])
+    return oracle.stack_forward(x, hosts, cfg["n_heads"], cfg["n_kv"], cfg["hd"])
+
+
+def test_stack_eager_graph_and_remap():
+    cfg, cap = SMALL, 16
+    stack, hosts, pool_bits, remap, n = _make_stack(cfg, 3, cap, 12)
+    assert n == 12
+    stack.forward()
+    torch.cuda.synchronize()
+    assert int(stack.status.item()) == 0
+    h_eager = stack.h.clone()
+    out_eager = stack.pool_out.clone()
+    ref = _oracle_stack(cfg, hosts, pool_bits, remap, n)
+    assert_parity(h_eager[:n].cpu().numpy(), ref, "stack eager")
+    assert not torch.any(h_eager[n:])                               # padding rows stay zero
+    assert torch.equal(stack.ybuf, h_eager.to(torch.bfloat16))      # narrow is RNE
+    got = host_bits(out_eager)
+    want = pool_bits.copy()
+    want[remap[:n]] = host_bits(stack.ybuf)[:n]
+    assert np.array_equal(got, want)                                 # only remapped rows change
+
+    # the captured graph replays the same step bit for bit
+    stack.capture()
+    stack.pool_out.copy_(stack.pool_in)
+    stack.h.fill_(123.0)
+    stack.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(stack.h, h_eager)
+    assert torch.equal(stack.pool_out, out_eager)
+
+    # a new batch: only the remap contents and n_active change, the graph stays valid
+    for n2 in (5, 1, cap):
+        perm = synth.permutation(9, n2, pool_bits.shape[0])[:cap].astype(np.int32)
+        stack.remap.copy_(torch.from_numpy(perm))
+        stack.n_active.fill_(n2)
+        stack.pool_out.copy_(stack.pool_in)
+        stack.replay()
+        torch.cuda.synchronize()
+        assert int(stack.status.item()) == 0
+        ref = _oracle_stack(cfg, hosts, pool_bits, perm, n2)
+        assert_parity(stack.h[:n2].cpu().numpy(), ref, "stack replay n=%d" % n2)
+        assert not torch.any(stack.h[n2:])
+    stack.destroy()
+
+
+def test_stack_launch_count():
+    stack, *_ = _make_stack(SMALL, 2, 8, 6)
+    assert stack.launch_count() == 4 + 2 * 11

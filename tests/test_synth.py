@@ -133,3 +133,12 @@ def test_paged_batch():
     assert sorted(used.tolist()) == list(range(total))
     for s in range(64):
         assert np.all(table[s, nb[s]:] == -1)
+
+
+def test_c_backend_matches_numpy_definition():
+    assert synth._host() is not None, "libsynth_host.so not built"
+    for shape, std, cs in [((33, 70), 0.37, None), ((16, 512), 1 / 8, synth.sigma_scale(512)),
+                           ((1, 5), 3.0, None)]:
+        tag = synth.make_tag(2, 6, synth.KIND_A)
+        assert np.array_equal(synth.bf16_normal(9, tag, shape, std, cs),
+                              synth.bf16_normal_numpy(9, tag, shape, std, cs))
