@@ -17,8 +17,9 @@ def _ensure_built():
     gen = os.path.join(ROOT, "synth", "libsynth.so")
     host = os.path.join(ROOT, "synth", "libsynth_host.so")
     if not (os.path.exists(lib) and os.path.exists(gen) and os.path.exists(host)):
-        from rank_decomposed_gb300 import build as _b
-        _b.build()
+        sys.path.insert(0, ROOT)
+        import __graft_entry__
+        __graft_entry__.build()
 
 
 _ensure_built()
