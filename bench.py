@@ -1,0 +1,487 @@
+"""Benchmark of the factorized-linear decode path on one GB300 (or N replicas).
+
+A step is one decode step of the whole path over one batch: remap_compact of
+the batch's active rows out of a paged pool, a 32-layer LLaMA-7B-shaped
+decomposed stack (q/k/v/o + SiLU-GLU MLP, every projection a rank-r factor
+pair at 40 % parameter reduction), and remap_scatter of the results, replayed
+as one CUDA graph.  Inputs are seeded synthetic data (7.75 GB of bf16 factors,
+far larger than L2, so every step streams them from HBM).
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on a
+bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+D, DFF, NH, NKV, HD = 4096, 11008, 32, 32, 128
+RHO = 0.4
+BLOCK_ROWS = 16
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def rank_for(d_in, d_out, rho):
+    """r = (1 - rho) d_in d_out / (d_in + d_out) rounded to the nearest multiple of 64."""
+    from fractions import Fraction
+    exact = (1 - Fraction(str(rho))) * d_in * d_out / (d_in + d_out)
+    return int(64 * max((exact / 64 + Fraction(1, 2)).__floor__(), 1))
+
+
+def shapes(rho=RHO):
+    io = [(D, NH * HD), (D, NKV * HD), (D, NKV * HD), (NH * HD, D), (D, DFF), (D, DFF), (DFF, D)]
+    return [(a, b, rank_for(a, b, rho)) for a, b in io]
+
+
+def linear_bytes(M, d_in, d_out, r):
+    """Algorithmic HBM bytes of one factorized linear: both factors plus x in and y out (bf16)."""
+    return 2 * r * (d_in + d_out) + 2 * M * (d_in + d_out)
+
+
+def step_bytes(M, n_layers, rho=RHO):
+    return n_layers * sum(linear_bytes(M, a, b, r) for a, b, r in shapes(rho))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        hbm = p.get("hbm_gbs")
+        tf = p.get("bf16_tflops_sustained") or p.get("bf16_tflops")
+        if hbm and tf:
+            return float(hbm), float(tf), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ------------------------------------------------------------------ inputs
+def batch(seed, n_seq, cap):
+    """Paged decode batch: lengths U{128..4096}, 16-row blocks, last row of each sequence."""
+    L, table, total = synth.paged_batch(seed, n_seq, 128, 4096, BLOCK_ROWS)
+    order = synth.permutation(seed, synth.make_tag(0, 2, synth.KIND_PERM), n_seq)
+    return L[order], table[order], total * BLOCK_ROWS
+
+
+class Clocks:
+    """nvidia-smi sampler run during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % index)
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- our arm
+class Workload:
+    def __init__(self, torch, lr, M, n_layers, seed=0, rho=RHO, n_seq=None):
+        self.torch, self.lr = torch, lr
+        self.M, self.n_layers, self.rho = M, n_layers, rho
+        dev = "cuda"
+        self.layers = []
+        cs_cache = {}
+        for l in range(n_layers):
+            fs = []
+            for p, (a, b, r) in enumerate(shapes(rho)):
+                sa, sg = synth.factor_stds(a, r)
+                At = torch.empty((r, a), dtype=torch.bfloat16, device=dev)
+                Bt = torch.empty((b, r), dtype=torch.bfloat16, device=dev)
+                if r not in cs_cache:
+                    cs_cache[r] = torch.from_numpy(synth.sigma_scale(r)).to(dev)
+                synth.fill_bf16_normal_device(At.data_ptr(), r, a, seed, synth.make_tag(l, p, synth.KIND_A), sa)
+                synth.fill_bf16_normal_device(Bt.data_ptr(), b, r, seed, synth.make_tag(l, p, synth.KIND_B), sg,
+                                              cs_cache[r].data_ptr())
+                fs.append(lr.FactorPair(At, Bt))
+            self.layers.append(lr.Block(D, DFF, NH, NKV, HD, fs))
+        torch.cuda.synchronize()
+        n_seq = M if n_seq is None else n_seq
+        self.lengths, self.table, pool_rows = batch(seed, n_seq, M)
+        pool = torch.empty((pool_rows, D), dtype=torch.bfloat16, device=dev)
+        synth.fill_bf16_normal_device(pool.data_ptr(), pool_rows, D, seed,
+                                      synth.make_tag(0, 0, synth.KIND_POOL), 1.0)
+        remap, n_active, self.n_runs = lr.remap_build(self.lengths, self.table, BLOCK_ROWS, 1, M)
+        self.stack = lr.Stack(
+            self.layers, pool, torch.empty_like(pool), torch.from_numpy(remap).to(dev),
+            torch.tensor([n_active], dtype=torch.int32, device=dev),
+            torch.zeros(M, D, dtype=torch.bfloat16, device=dev),
+            torch.zeros(M, D, dtype=torch.float32, device=dev),
+            torch.zeros(M, D, dtype=torch.bfloat16, device=dev),
+            torch.zeros(lr.Stack.scratch_bytes(M, self.layers), dtype=torch.uint8, device=dev),
+            torch.zeros(1, dtype=torch.int32, device=dev))
+        self.n_active = n_active
+
+    def free(self):
+        self.stack.destroy()
+
+
+def time_graph(torch, stack, steps, warmup, clocks=None, barrier=None):
+    for _ in range(warmup):
+        stack.replay()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(s)
+    for _ in range(steps):
+        stack.replay(s)
+    e1.record(s)
+    torch.cuda.synchronize()
+    ck = clocks.stop() if clocks else None
+    if barrier:
+        barrier()
+    return e0.elapsed_time(e1) / steps, ck
+
+
+def time_eager(torch, stack, steps, warmup):
+    for _ in range(warmup):
+        stack.forward()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        stack.forward()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def time_e2e(torch, lr, w, steps, warmup):
+    """Host-driven steps: host remap scan, pinned H2D of the remap, graph replay, D2H of the rows."""
+    st = w.stack
+    cap = w.M
+    remap_h = torch.empty(cap, dtype=torch.int32, pin_memory=True)
+    nact_h = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    out_h = torch.empty((cap, D), dtype=torch.bfloat16, pin_memory=True)
+    rh, nh = remap_h.numpy(), nact_h.numpy()
+
+    def one():
+        remap, n, _ = lr.remap_build(w.lengths, w.table, BLOCK_ROWS, 1, cap)
+        rh[:] = remap
+        nh[0] = n
+        st.remap.copy_(remap_h, non_blocking=True)
+        st.n_active.copy_(nact_h, non_blocking=True)
+        st.replay()
+        out_h.copy_(st.ybuf, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = (time.perf_counter() - t0) / steps
+    return dt, remap_h.numel() * 4 + 4, out_h.numel() * 2
+
+
+def time_linears(torch, lr, w, reps=3):
+    """Event-timed decode linears (down + up launch each) over every layer's 7 projections.
+
+    The stream is first held busy by a fixed-length GPU sleep so that all the
+    launches and events are queued before the GPU reaches them: the event
+    pairs then bracket only the kernels.  Returns (sum of algorithmic bytes,
+    sum of times in s, launches, per-projection GB/s).
+    """
+    M = w.M
+    x = torch.empty((M, DFF), dtype=torch.bfloat16, device="cuda")
+    synth.fill_bf16_normal_device(x.data_ptr(), M, DFF, 1, synth.make_tag(0, 0, synth.KIND_X), 1.0)
+    y = torch.empty((M, DFF), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(max(lr.linear_workspace_bytes(M, f) for f in w.layers[0].factors),
+                     dtype=torch.uint8, device="cuda")
+    calls = [(p, f) for b in w.layers for p, f in enumerate(b.factors)]
+    n = len(calls)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    for p, f in calls[:7]:
+        lr.linear_forward(x[:, : f.d_in], f, y[:, : f.d_out], ws, None)
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        torch.cuda._sleep(100_000_000)          # ~50 ms of GPU time while the host queues
+        for i, (p, f) in enumerate(calls):
+            evs[i].record()
+            lr.linear_forward(x[:, : f.d_in], f, y[:, : f.d_out], ws, None)
+        evs[n].record()
+        torch.cuda.synchronize()
+        times = [evs[i].elapsed_time(evs[i + 1]) * 1e-3 for i in range(n)]
+        tot = sum(times)
+        if best is None or tot < best[0]:
+            best = (tot, times)
+    tot, times = best
+    nbytes = [linear_bytes(M, f.d_in, f.d_out, f.r) for _, f in calls]
+    per_proj = {}
+    for (p, f), t, bb in zip(calls, times, nbytes):
+        k = synth.PROJ_NAMES[p]
+        a, c = per_proj.get(k, (0.0, 0.0))
+        per_proj[k] = (a + bb, c + t)
+    return float(sum(nbytes)), float(tot), 2 * n, {k: round(v[0] / v[1] / 1e9, 1) for k, v in per_proj.items()}
+
+
+def time_prefill(torch, lr, M=16384, rhos=(0.2, 0.4, 0.6), reps=3):
+    """Config-2 prefill: the 7 projections of one 7B layer at M rows, per rank sweep."""
+    out = {}
+    x = torch.empty((M, DFF), dtype=torch.bfloat16, device="cuda")
+    synth.fill_bf16_normal_device(x.data_ptr(), M, DFF, 2, synth.make_tag(0, 0, synth.KIND_X), 1.0)
+    y = torch.empty((M, DFF), dtype=torch.bfloat16, device="cuda")
+    for rho in rhos:
+        fs = []
+        for p, (a, b, r) in enumerate(shapes(rho)):
+            sa, sg = synth.factor_stds(a, r)
+            At = torch.empty((r, a), dtype=torch.bfloat16, device="cuda")
+            Bt = torch.empty((b, r), dtype=torch.bfloat16, device="cuda")
+            cs = torch.from_numpy(synth.sigma_scale(r)).cuda()
+            synth.fill_bf16_normal_device(At.data_ptr(), r, a, 3, synth.make_tag(0, p, synth.KIND_A), sa)
+            synth.fill_bf16_normal_device(Bt.data_ptr(), b, r, 3, synth.make_tag(0, p, synth.KIND_B), sg, cs.data_ptr())
+            fs.append(lr.FactorPair(At, Bt))
+        ws = torch.zeros(max(lr.linear_workspace_bytes(M, f) for f in fs), dtype=torch.uint8, device="cuda")
+        flops = sum(2.0 * M * f.r * (f.d_in + f.d_out) for f in fs)
+        for f in fs:
+            lr.linear_forward(x[:, : f.d_in], f, y[:, : f.d_out], ws, None)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for f in fs:
+                lr.linear_forward(x[:, : f.d_in], f, y[:, : f.d_out], ws, None)
+            e1.record()
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) * 1e-3
+            best = t if best is None else min(best, t)
+        out[str(rho)] = {"ranks": [f.r for f in fs], "ms_per_layer": round(best * 1e3, 3),
+                         "tokens_per_s_32_layers": round(M / (best * 32), 1),
+                         "tflops": round(flops / best / 1e12, 1)}
+        del fs, ws
+        torch.cuda.empty_cache()
+    return out
+
+
+def oracle_sample(M, layers_sample, seed=0, rho=RHO):
+    """Time the fp64 oracle on M rows through `layers_sample` layers (factor generation untimed)."""
+    import oracle
+    L, table, pool_rows = batch(seed, M, M)
+    remap, n, _ = oracle.remap_build(L, table, BLOCK_ROWS, 1, M)
+    # the active rows of the pool, regenerated element-exactly from their stream offsets
+    key = synth.stream_key(seed, synth.make_tag(0, 0, synth.KIND_POOL))
+    x = np.stack([synth.f64_to_bf16_bits(synth.normal_f64(key, D, start=int(j) * D)) for j in remap[:n]])
+    h = oracle.widen_bf16(x)
+    total = 0.0
+    for l in range(layers_sample):
+        fac = {}
+        for p, (a, b, r) in enumerate(shapes(rho)):
+            At, Bt = synth.factor_pair(seed, l, p, a, b, r)
+            fac[synth.PROJ_NAMES[p]] = oracle.factor_from_stored(At, Bt)
+        t0 = time.perf_counter()
+        h = oracle.block_forward(h, fac, NH, NKV, HD)
+        total += time.perf_counter() - t0
+    return total, n
+
+
+def cpu_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = max((i.get("num_threads", 0) for i in info), default=0)
+        if n:
+            return int(n)
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--M", type=int, default=64)
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--no-extras", action="store_true", help="skip the M sweep, eager and prefill legs")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    workload = ("LLaMA-7B-shaped 32-layer decomposed stack (rho=0.4; q/k/v/o r=1216, gate/up/down "
+                "r=1792), decode M=%d rows compacted by remap from a paged pool, CUDA-graph replay"
+                % args.M) if args.layers == 32 else "LLaMA-7B-shaped %d-layer stack, M=%d" % (args.layers, args.M)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, workload)
+        return
+
+    import torch
+    import rank_decomposed_gb300 as lr
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    else:
+        torch.cuda.set_device(0)
+    barrier = (lambda: dist.barrier()) if dist else None
+
+    w = Workload(torch, lr, args.M, args.layers, seed=rank)
+    w.stack.capture()
+    clocks = Clocks(torch.cuda.current_device() if world == 1 else local)
+    ms, ck = time_graph(torch, w.stack, args.steps, args.warmup, clocks, barrier)
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if int(w.stack.status.item()) != 0:
+        raise SystemExit("device status %d" % int(w.stack.status.item()))
+    tokens = args.M * world
+    value = tokens / (ms * 1e-3)
+    launches = w.stack.launch_count() * args.steps
+
+    hbm, tf, peak_kind = load_peaks()
+    line = {
+        "metric": "factorized-linear tokens/s (decode)",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload, "model": "llama-7b-shaped factorized stack (random factors)",
+                   "global_batch": tokens, "seq_len": 1, "rows_per_gpu": args.M,
+                   "layers": args.layers, "rho": RHO, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2: %.2f GB of factors streamed per step" % (step_bytes(args.M, args.layers) / 1e9),
+                   "remap_runs": w.n_runs},
+        "clocks": ck, "gpu_launches": launches,
+        "step_hbm_gbs": round(step_bytes(args.M, args.layers) / (ms * 1e-3) / 1e9, 1),
+    }
+    if rank == 0:
+        e2e_s, bi, bo = time_e2e(torch, lr, w, max(5, args.steps // 2), 3)
+        line["e2e"] = {"value": round(tokens / e2e_s, 1), "unit": "tokens/s",
+                       "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+                       "ms_per_step": round(e2e_s * 1e3, 4),
+                       "path": "host remap_build + pinned H2D of remap/n_active + graph replay + D2H of the step's rows"}
+        nbytes, tsum, nl, per_proj = time_linears(torch, lr, w)
+        achieved = nbytes / tsum / 1e9
+        line["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                            "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": peak_kind,
+                            "kernel": "decode_kernel (tcgen05 swap-AB), down+up launches of every linear",
+                            "launches_timed": nl, "avg_launch_us": round(tsum / nl * 1e6, 2),
+                            "algorithmic_bytes_per_launch": round(nbytes / nl),
+                            "per_projection_gbs": per_proj}
+        if not args.no_extras:
+            line["graph_vs_eager"] = {"graph_ms": round(ms, 4),
+                                      "eager_ms": round(time_eager(torch, w.stack, 5, 3), 4)}
+        w.free()
+        del w
+        torch.cuda.empty_cache()
+        if not args.no_extras:
+            sweep = {}
+            for M in (1, 8, 32, 64):
+                ww = Workload(torch, lr, M, args.layers, seed=0)
+                ww.stack.capture()
+                t, _ = time_graph(torch, ww.stack, max(10, args.steps // 2), 3)
+                sweep[str(M)] = {"ms_per_step": round(t, 4), "tokens_per_s": round(M / (t * 1e-3), 1),
+                                 "step_hbm_gbs": round(step_bytes(M, args.layers) / (t * 1e-3) / 1e9, 1)}
+                ww.free()
+                del ww
+                torch.cuda.empty_cache()
+            line["decode_sweep"] = sweep
+            pre = time_prefill(torch, lr)
+            for v in pre.values():
+                v["frac_of_bf16_peak"] = round(v["tflops"] / tf, 4)
+            line["prefill"] = pre
+        if not args.no_cpu:
+            sample_layers = min(8, args.layers)
+            tcpu, n = oracle_sample(args.M, sample_layers)
+            v = n / (tcpu * args.layers / sample_layers)
+            line["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": cpu_threads(),
+                                    "kind": "oracle",
+                                    "sample": "fp64 oracle over the same %d rows through %d of %d layers "
+                                              "(%.1f s), scaled linearly to the full stack" % (n, sample_layers, args.layers, tcpu)}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args, workload):
+    """The oracle as it stands, on the host cores: each step is 1 layer of the stack for M rows."""
+    import oracle  # noqa: F401
+    for _ in range(args.warmup):
+        oracle_sample(args.M, 1)
+    tot, n = 0.0, 0
+    for _ in range(args.steps):
+        t, n = oracle_sample(args.M, 1)
+        tot += t
+    per_layer = tot / args.steps
+    value = n / (per_layer * args.layers)
+    line = {"impl": "reference", "metric": "factorized-linear tokens/s (decode)", "value": round(value, 3),
+            "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(per_layer * args.layers * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload, "rows": n, "layers": args.layers, "rho": RHO},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": "each step: the fp64 oracle on %d rows through 1 of %d layers, "
+                                       "scaled linearly to the full stack" % (n, args.layers)},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -58,11 +58,18 @@ __device__ __forceinline__ int act_col(const DecodeProblem& P, int kb) {
   return k;
 }
 
-__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
   uint32_t remote;
-  float v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  return remote;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
   return v;
 }
 
@@ -72,15 +79,34 @@ __device__ __forceinline__ void cluster_sync_all() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void store_out(const DecodeProblem& P, int m, int n, float v) {
+// Four consecutive outputs (m, n .. n+3) of one problem.
+__device__ __forceinline__ void store_out4(const DecodeProblem& P, int m, int n, float4 v) {
   const int64_t off = static_cast<int64_t>(m) * P.ldo + n;
   if (P.epi == EPI_STORE_BF16) {
-    static_cast<uint16_t*>(P.out)[off] = f32_to_bf16_rn(v);
-  } else if (P.epi == EPI_STORE_F32) {
-    static_cast<float*>(P.out)[off] = v;
+    uint16_t* o = static_cast<uint16_t*>(P.out) + off;
+    const uint16_t b0 = f32_to_bf16_rn(v.x), b1 = f32_to_bf16_rn(v.y);
+    const uint16_t b2 = f32_to_bf16_rn(v.z), b3 = f32_to_bf16_rn(v.w);
+    if (P.vec_ok) {
+      *reinterpret_cast<uint2*>(o) = make_uint2(static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16),
+                                                static_cast<uint32_t>(b2) | (static_cast<uint32_t>(b3) << 16));
+    } else {
+      o[0] = b0; o[1] = b1; o[2] = b2; o[3] = b3;
+    }
   } else {
     float* o = static_cast<float*>(P.out) + off;
-    *o = *o + v;
+    if (P.epi == EPI_ADD_F32) {
+      if (P.vec_ok) {
+        const float4 h = *reinterpret_cast<const float4*>(o);
+        v.x += h.x; v.y += h.y; v.z += h.z; v.w += h.w;
+      } else {
+        v.x += o[0]; v.y += o[1]; v.z += o[2]; v.w += o[3];
+      }
+    }
+    if (P.vec_ok) {
+      *reinterpret_cast<float4*>(o) = v;
+    } else {
+      o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+    }
   }
 }
 
@@ -229,18 +255,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();  // every partial tile of the cluster is in shared memory
 
   if (warp >= 2) {
+    // Reduce this CTA's share of the tile -- tokens [t0, t1) x 128 rows -- over
+    // the S partial tiles of the cluster, in rank order, four rows at a time.
     pdl_wait();  // outputs (e.g. the residual stream) belong to earlier kernels
-    const int row = (warp & 3) * 32 + lane;
-    const int n = n0 + row;
+    const int et = threadIdx.x - 64;
     const int t0 = split * p.M / S;
     const int t1 = (split + 1) * p.M / S;
-    if (n < P.N) {
-      for (int tok = t0; tok < t1; ++tok) {
-        const float* src = ptile + tok * kTileN + row;
-        float acc = 0.f;
-        for (int s2 = 0; s2 < S; ++s2) acc += ld_cluster_f32(src, static_cast<uint32_t>(s2));
-        store_out(P, tok, n, acc);
-      }
+    const int nchunks = (t1 - t0) * (kTileN / 4);
+    const uint32_t pbase = smem_u32(ptile);
+    uint32_t rbase[kMaxCluster];
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxCluster; ++s2)
+      rbase[s2] = s2 < S ? cluster_addr(pbase, static_cast<uint32_t>(s2)) : 0u;
+    for (int c = et; c < nchunks; c += 128) {
+      const int tok = t0 + c / (kTileN / 4);
+      const int row = (c % (kTileN / 4)) * 4;
+      if (n0 + row >= P.N) continue;  // N is a multiple of 64: the 4 rows are all in or all out
+      const uint32_t off = static_cast<uint32_t>((tok * kTileN + row) * 4);
+      float4 v[kMaxCluster];
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxCluster; ++s2)
+        if (s2 < S) v[s2] = ld_cluster_f32x4(rbase[s2] + off);
+      float4 acc = v[0];
+#pragma unroll
+      for (int s2 = 1; s2 < kMaxCluster; ++s2)
+        if (s2 < S) {
+          acc.x += v[s2].x;
+          acc.y += v[s2].y;
+          acc.z += v[s2].z;
+          acc.w += v[s2].w;
+        }
+      store_out4(P, tok, n0 + row, acc);
     }
   }
 
@@ -329,6 +374,7 @@ lr_status launch_nt(int M, const GemmOp* ops, int n_ops, int32_t* status, cudaSt
     P.epi = o.epi;
     P.out = o.out;
     P.ldo = o.ldo;
+    P.vec_ok = (reinterpret_cast<uintptr_t>(o.out) % 16 == 0) && (o.ldo % 8 == 0) ? 1 : 0;
     items += P.n_tiles * S;
   }
   cudaLaunchConfig_t cfg;

@@ -12,8 +12,10 @@
 namespace lr {
 namespace {
 
-// Launch with programmatic dependent launch when enabled; every kernel here
-// calls pdl_wait() before it touches memory written by earlier kernels.
+// Launch with programmatic dependent launch when enabled.  Every kernel here
+// lets its dependents launch first (they only prefetch weights before their
+// own wait) and calls pdl_wait() before it touches memory written by earlier
+// kernels.
 template <typename... KArgs, typename... Args>
 lr_status launch(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t s, const char* what,
                  Args... args) {
@@ -47,8 +49,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ p
                                                      const int32_t* __restrict__ n_active,
                                                      uint4* __restrict__ buf, int64_t cap,
                                                      int32_t* status) {
-  pdl_wait();
   pdl_launch_dependents();
+  pdl_wait();
   const int64_t i = blockIdx.x;
   const int n = clamp_active(n_active, cap);
   uint4* dst = buf + i * row_vecs;
@@ -76,8 +78,8 @@ __global__ void __launch_bounds__(256) scatter_kernel(const uint4* __restrict__ 
                                                       uint4* __restrict__ pool, int64_t pool_rows,
                                                       int64_t row_vecs, int64_t cap,
                                                       int32_t* status) {
-  pdl_wait();
   pdl_launch_dependents();
+  pdl_wait();
   const int64_t i = blockIdx.x;
   const int n = clamp_active(n_active, cap);
   if (i >= n) return;
@@ -94,8 +96,8 @@ __global__ void __launch_bounds__(256) scatter_kernel(const uint4* __restrict__ 
 // out[m] = bf16(h[m] / sqrt(mean(h[m]^2) + eps)); one CTA per row.
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float4* __restrict__ h,
                                                       uint2* __restrict__ out, int d4, float eps) {
-  pdl_wait();
   pdl_launch_dependents();
+  pdl_wait();
   __shared__ float part[8];
   const int64_t row = blockIdx.x;
   const float4* x = h + row * d4;
@@ -130,8 +132,8 @@ __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z));
 __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__ g,
                                                        const uint4* __restrict__ u,
                                                        uint4* __restrict__ a, int64_t n8) {
-  pdl_wait();
   pdl_launch_dependents();
+  pdl_wait();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint4 gv = g[i];
@@ -154,8 +156,8 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__
 
 __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ in,
                                                     float4* __restrict__ out, int64_t n8) {
-  pdl_wait();
   pdl_launch_dependents();
+  pdl_wait();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint4 v = in[i];
@@ -168,8 +170,8 @@ __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ in
 
 __global__ void __launch_bounds__(256) narrow_kernel(const float4* __restrict__ in,
                                                      uint4* __restrict__ out, int64_t n8) {
-  pdl_wait();
   pdl_launch_dependents();
+  pdl_wait();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float4 a = in[2 * i];

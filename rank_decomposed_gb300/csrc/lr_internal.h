@@ -54,7 +54,7 @@ struct DecodeProblem {
   int32_t gqa_head_dim;
   int32_t gqa_group;
   int32_t epi;
-  int32_t pad_;
+  int32_t vec_ok;       // out 16-byte aligned and ldo % 8 == 0: vector stores
   void* out;
   int64_t ldo;
 };
