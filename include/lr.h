@@ -115,6 +115,35 @@ lr_status lr_linear_forward(const void* x, int64_t ldx, void* y, int64_t ldy, lr
                             int32_t* dev_status, lr_stream s);
 
 /* ---------------------------------------------------------------------------
+ * lr_linear_forward_noalloc: the same computation as lr_linear_forward for
+ * callers that cannot allocate device memory.  The paper has no counterpart;
+ * this is an interface convenience.
+ *   Some callers cannot hand the library a workspace: code that runs where
+ *   cudaMalloc is forbidden or unwanted (an allocator-free embedded runtime, a
+ *   plugin that receives only raw pointers and a stream, a serving loop whose
+ *   device memory is fixed at start-up), or code that must not risk the
+ *   implicit device synchronisation an allocation can cause.  This entry point
+ *   keeps the intermediate t = x A_r in a static device array of
+ *   LR_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library instead.  Every GPU
+ *   that loads the library holds that array until the process exits.  The
+ *   call itself allocates nothing (no cudaMalloc/cudaFree, no allocating
+ *   library routine).
+ *   Arguments, layouts, checks and results are those of lr_linear_forward
+ *   without the workspace.  M * r * 2 must not exceed LR_NOALLOC_SCRATCH_BYTES;
+ *   larger problems are rejected with LR_ERR_UNSUPPORTED and a message in
+ *   lr_last_error().
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   All calls share the one array and it keeps the last call's contents.
+ *   Nothing in it needs to start at zero (each call writes every element it
+ *   reads).  Calls that overlap on the GPU (on different streams, say) race on
+ *   it: order them on one stream. */
+#define LR_NOALLOC_SCRATCH_BYTES (4u << 20)
+lr_status lr_linear_forward_noalloc(const void* x, int64_t ldx, void* y, int64_t ldy,
+                                    lr_dtype y_dtype, int64_t M, const lr_factor* f,
+                                    int32_t* dev_status, lr_stream s);
+
+/* ---------------------------------------------------------------------------
  * lr_block_forward: one decomposed block applied in place to the fp32 residual
  * stream h (device fp32 [M][d_model], 16-byte aligned):
  *   n1 = RMSNorm(h); q,k,v = LR(n1); h += LR_o(attn(v));

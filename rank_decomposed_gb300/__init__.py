@@ -67,6 +67,7 @@ def _load():
     sig = {
         "lr_linear_workspace_bytes": (sz, [i64, P(Factor)]),
         "lr_linear_forward": (i32, [vp, i64, vp, i64, i32, i64, P(Factor), vp, sz, vp, vp]),
+        "lr_linear_forward_noalloc": (i32, [vp, i64, vp, i64, i32, i64, P(Factor), vp, vp]),
         "lr_block_scratch_bytes": (sz, [i64, P(BlockDesc)]),
         "lr_block_forward": (i32, [vp, i64, P(BlockDesc), vp, sz, vp, vp]),
         "remap_compact": (i32, [vp, i64, i64, vp, vp, vp, i64, vp, vp]),
@@ -189,6 +190,29 @@ def linear_forward(x, f: FactorPair, y, workspace, status, stream=None):
                                workspace.numel() * workspace.element_size(), _ptr(status),
                                _stream(stream))
     _check("lr_linear_forward", st)
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def linear_forward_noalloc(x, f: FactorPair, y, status, stream=None):
+    """y = (x A_r) B_r with the intermediate kept in the library's static device array.
+
+    For callers that cannot allocate device memory: no workspace argument and
+    no allocation.  Requires M * r * 2 <= NOALLOC_SCRATCH_BYTES; calls that
+    overlap on the GPU share the array and must be ordered on one stream.
+    """
+    import torch
+    _bf16(x, "x")
+    if y.dim() != 2 or y.stride(1) != 1:
+        raise ValueError("y must be a row-major 2-D tensor")
+    ydt = {torch.bfloat16: LR_BF16, torch.float32: LR_F32}.get(y.dtype)
+    if ydt is None:
+        raise TypeError("y must be bfloat16 or float32")
+    fc = f.c()
+    st = lib.lr_linear_forward_noalloc(x.data_ptr(), x.stride(0), y.data_ptr(), y.stride(0), ydt,
+                                       x.shape[0], ctypes.byref(fc), _ptr(status), _stream(stream))
+    _check("lr_linear_forward_noalloc", st)
 
 
 # ---------------------------------------------------------------- block
