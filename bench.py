@@ -124,7 +124,7 @@ class Clocks:
 
 # -------------------------------------------------------------- our arm
 class Workload:
-    def __init__(self, torch, lr, M, n_layers, seed=0, rho=RHO, n_seq=None):
+    def __init__(self, torch, lr, M, n_layers, seed=0, rho=RHO, n_seq=None, mode=0):
         self.torch, self.lr = torch, lr
         self.M, self.n_layers, self.rho = M, n_layers, rho
         dev = "cuda"
@@ -156,8 +156,8 @@ class Workload:
             torch.zeros(M, D, dtype=torch.bfloat16, device=dev),
             torch.zeros(M, D, dtype=torch.float32, device=dev),
             torch.zeros(M, D, dtype=torch.bfloat16, device=dev),
-            torch.zeros(lr.Stack.scratch_bytes(M, self.layers), dtype=torch.uint8, device=dev),
-            torch.zeros(1, dtype=torch.int32, device=dev))
+            torch.zeros(lr.Stack.scratch_bytes(M, self.layers, mode), dtype=torch.uint8, device=dev),
+            torch.zeros(1, dtype=torch.int32, device=dev), mode=mode)
         self.n_active = n_active
 
     def free(self):
@@ -425,8 +425,20 @@ def main():
                             "algorithmic_bytes_per_launch": round(nbytes / nl),
                             "per_projection_gbs": per_proj}
         if not args.no_extras:
-            line["graph_vs_eager"] = {"graph_ms": round(ms, 4),
-                                      "eager_ms": round(time_eager(torch, w.stack, 5, 3), 4)}
+            # the analogue of the pages' CUDA-graph ablation: the same step
+            # replayed as a graph, enqueued eagerly, and as one persistent kernel
+            eager_ms = time_eager(torch, w.stack, 5, 3)
+            cmp = {"graph_ms": round(ms, 4), "eager_ms": round(eager_ms, 4),
+                   "launches_per_step": w.stack.launch_count()}
+            w.stack.destroy()
+            w.stack.mode = lr.STACK_PERSISTENT
+            w.stack._desc = None
+            need = lr.Stack.scratch_bytes(args.M, w.layers, lr.STACK_PERSISTENT)
+            w.stack.scratch = torch.zeros(need, dtype=torch.uint8, device="cuda")
+            w.stack.capture()
+            pers_ms, _ = time_graph(torch, w.stack, 10, 3)
+            cmp["persistent_graph_ms"] = round(pers_ms, 4)
+            line["graph_vs_eager"] = cmp
         w.free()
         del w
         torch.cuda.empty_cache()

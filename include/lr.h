@@ -84,7 +84,7 @@ enum { LR_Q = 0, LR_K = 1, LR_V = 2, LR_O = 3, LR_GATE = 4, LR_UP = 5, LR_DOWN =
  * q: d_model -> n_heads*head_dim, k/v: d_model -> n_kv_heads*head_dim,
  * o: n_heads*head_dim -> d_model, gate/up: d_model -> d_ff, down: d_ff -> d_model.
  * n_heads must be a multiple of n_kv_heads (MHA, GQA, MQA); head_dim a multiple
- * of 64; RMSNorm has unit gain and the given eps. */
+ * of 64; d_model at most 8192; RMSNorm has unit gain and the given eps. */
 typedef struct {
   int32_t d_model;
   int32_t d_ff;
@@ -205,6 +205,7 @@ lr_status remap_build(const int32_t* lengths, int64_t n_seq, const int32_t* bloc
  * scratch: max over layers of lr_block_scratch_bytes(cap, layer).
  * All layers must share d_model.  Rows i >= *n_active run through the layers
  * as zero rows and are not scattered. */
+enum { LR_STACK_AUTO = 0, LR_STACK_LAYERED = 1, LR_STACK_PERSISTENT = 2 };
 typedef struct {
   int32_t n_layers;
   const lr_block_desc* layers; /* host array [n_layers]; copied by the calls */
@@ -220,9 +221,21 @@ typedef struct {
   void* scratch;
   size_t scratch_bytes;
   int32_t* dev_status;
+  /* LR_STACK_AUTO / LR_STACK_LAYERED: one launch per kernel, chained by
+   * programmatic dependent launch.  LR_STACK_PERSISTENT (cap <= 256): the
+   * whole step as one cooperative kernel, one CTA per SM walking a program
+   * of phases separated by grid barriers. */
+  int32_t mode;
 } lr_stack_desc;
 
-/* Enqueue one step eagerly (one launch per kernel). */
+/* Scratch the step needs: the block buffers plus, in persistent mode, the
+ * step's program (tensor maps, phases, work segments), split-K partials and
+ * counters.  Uses only n_layers, layers, cap and mode of the descriptor.
+ * A captured graph keeps using its scratch until lr_graph_destroy. */
+size_t lr_stack_scratch_bytes(const lr_stack_desc* st);
+
+/* Enqueue one step eagerly.  In persistent mode the program is rebuilt and
+ * copied to the scratch first (the call waits for that copy on stream s). */
 lr_status lr_stack_forward(const lr_stack_desc* st, lr_stream s);
 
 /* Capture one step into a CUDA graph owned by the library (captured on a
@@ -234,7 +247,8 @@ lr_status lr_graph_capture(const lr_stack_desc* st, lr_graph** out);
 lr_status lr_graph_replay(lr_graph* g, lr_stream s);
 lr_status lr_graph_destroy(lr_graph* g);
 
-/* Number of kernel launches one step enqueues (eager or in the graph). */
+/* Number of kernel launches one step enqueues (eager or in the graph):
+ * 1 in persistent mode. */
 int64_t lr_stack_launch_count(const lr_stack_desc* st);
 
 const char* lr_status_string(lr_status st);

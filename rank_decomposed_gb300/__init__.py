@@ -54,7 +54,12 @@ class StackDesc(ctypes.Structure):
                 ("n_active", ctypes.c_void_p), ("cap", ctypes.c_int64),
                 ("xbuf", ctypes.c_void_p), ("h", ctypes.c_void_p), ("ybuf", ctypes.c_void_p),
                 ("scratch", ctypes.c_void_p), ("scratch_bytes", ctypes.c_size_t),
-                ("dev_status", ctypes.c_void_p)]
+                ("dev_status", ctypes.c_void_p), ("mode", ctypes.c_int32)]
+
+
+STACK_AUTO = 0
+STACK_LAYERED = 1
+STACK_PERSISTENT = 2
 
 
 def _load():
@@ -78,6 +83,7 @@ def _load():
         "lr_graph_replay": (i32, [vp, vp]),
         "lr_graph_destroy": (i32, [vp]),
         "lr_stack_launch_count": (i64, [P(StackDesc)]),
+        "lr_stack_scratch_bytes": (sz, [P(StackDesc)]),
         "lr_status_string": (ctypes.c_char_p, [i32]),
         "lr_last_error": (ctypes.c_char_p, []),
     }
@@ -277,6 +283,7 @@ class Stack:
     ybuf: object
     scratch: object
     status: object
+    mode: int = STACK_AUTO
     _graph: object = field(default=None, repr=False)
     _desc: object = field(default=None, repr=False)
     _blocks: object = field(default=None, repr=False)
@@ -295,12 +302,20 @@ class Stack:
             d.scratch = self.scratch.data_ptr()
             d.scratch_bytes = self.scratch.numel() * self.scratch.element_size()
             d.dev_status = _ptr(self.status)
+            d.mode = self.mode
             self._blocks, self._desc = arr, d
         return self._desc
 
     @staticmethod
-    def scratch_bytes(cap: int, layers) -> int:
-        return max(block_scratch_bytes(cap, b) for b in layers)
+    def scratch_bytes(cap: int, layers, mode: int = STACK_AUTO) -> int:
+        """Scratch bytes of a step over `cap` rows (block buffers + persistent program)."""
+        arr = (BlockDesc * len(layers))(*[b.c() for b in layers])
+        d = StackDesc()
+        d.n_layers = len(layers)
+        d.layers = ctypes.cast(arr, ctypes.POINTER(BlockDesc))
+        d.cap = cap
+        d.mode = mode
+        return int(lib.lr_stack_scratch_bytes(ctypes.byref(d)))
 
     def launch_count(self) -> int:
         return int(lib.lr_stack_launch_count(ctypes.byref(self.desc())))

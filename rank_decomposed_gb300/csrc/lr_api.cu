@@ -113,6 +113,8 @@ lr_status ensure_configured() {
   if (st != LR_OK) return st;
   st = configure_prefill();
   if (st != LR_OK) return st;
+  st = configure_persist();
+  if (st != LR_OK) return st;
   done[dev] = true;
   return LR_OK;
 }
@@ -215,6 +217,10 @@ lr_status check_block(const lr_block_desc* b) {
     set_error("block: d_model, d_ff and head_dim must be multiples of 64");
     return LR_ERR_UNSUPPORTED;
   }
+  if (d > 8192) {
+    set_error("block: d_model above 8192 is not supported (RMSNorm keeps a row in registers)");
+    return LR_ERR_UNSUPPORTED;
+  }
   if (!(b->eps >= 0.f)) return invalid("block: eps must be >= 0");
   const int dq = b->n_heads * hd, dkv = b->n_kv_heads * hd;
   const int want[7][2] = {{d, dq}, {d, dkv}, {d, dkv}, {dq, d}, {d, dff}, {d, dff}, {dff, d}};
@@ -297,12 +303,276 @@ int64_t block_launches(int64_t M, const lr_block_desc*) {
 }
 
 // ---------------------------------------------------------------- stack
+bool use_persist(const lr_stack_desc* st) {
+  return st->mode == LR_STACK_PERSISTENT && st->cap <= persist_max_rows();
+}
+
+size_t block_region_bytes(const lr_stack_desc* st) {
+  size_t need = 0;
+  for (int l = 0; l < st->n_layers; ++l)
+    need = std::max(need, block_layout(st->cap, &st->layers[l]).total);
+  return align_up(need);
+}
+
+// Weight tiles (16 KB each) a CTA keeps requested into L2 beyond its shared-
+// memory ring.  152 CTAs x 32 tiles = 78 MB in flight or resident in L2.
+int persist_prefetch_tiles() {
+  static const int v = [] {
+    const char* e = getenv("LR_PERSIST_PREFETCH");
+    return (e && *e) ? atoi(e) : 32;
+  }();
+  return v;
+}
+
+int pick_nt(int64_t cap) {
+  return cap <= 16 ? 16 : cap <= 32 ? 32 : cap <= 64 ? 64 : cap <= 128 ? 128 : 256;
+}
+
+// Host-side program of the persistent decode step (see lr_persist.cu).
+struct MapReq {
+  const void* ptr;
+  uint64_t rows, cols, ld;
+  uint32_t box_rows;
+};
+
+struct Plan {
+  int G = 0, nt = 0, M = 0;
+  std::vector<PPhase> phases;
+  std::vector<PProblem> probs;
+  std::vector<MapReq> maps;
+  std::vector<std::vector<PSeg>> per_cta;
+  int n_ctr = 0;
+  int max_slots = 0;
+  // layout of the persistent region
+  size_t off_maps = 0, off_phases = 0, off_probs = 0, off_segs = 0, off_begin = 0;
+  size_t off_partials = 0, off_zero = 0, zero_bytes = 0, total = 0, n_segs = 0;
+};
+
+int add_map(Plan& P, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box) {
+  P.maps.push_back(MapReq{ptr, rows, cols, ld, box});
+  return static_cast<int>(P.maps.size()) - 1;
+}
+
+void add_glue(Plan& P, int kind, int d, const void* s0, const void* s1, void* d0, void* d1,
+              float eps) {
+  PPhase ph;
+  memset(&ph, 0, sizeof(ph));
+  ph.kind = kind;
+  ph.d = d;
+  ph.src0 = s0;
+  ph.src1 = s1;
+  ph.dst0 = d0;
+  ph.dst1 = d1;
+  ph.eps = eps;
+  P.phases.push_back(ph);
+}
+
+// A GEMM phase: its (tile, k-block) units are dealt out stream-K style, CTA c
+// taking units [c U / G, (c + 1) U / G).
+void add_gemm(Plan& P, const GemmOp* ops, int n_ops) {
+  const int phase = static_cast<int>(P.phases.size());
+  add_glue(P, PH_GEMM, 0, nullptr, nullptr, nullptr, nullptr, 0.f);
+  const int prob0 = static_cast<int>(P.probs.size());
+  std::vector<int64_t> ubase(n_ops + 1, 0);
+  std::vector<int> tiles(n_ops), nkb(n_ops);
+  for (int g = 0; g < n_ops; ++g) {
+    const GemmOp& o = ops[g];
+    PProblem pr;
+    memset(&pr, 0, sizeof(pr));
+    pr.wmap = add_map(P, o.W, o.N, o.K, o.ldw, 128);
+    pr.amap = add_map(P, o.act, P.M, o.act_cols, o.ld_act, P.nt);
+    pr.N = o.N;
+    pr.nkb = o.K / 64;
+    pr.epi = o.epi;
+    pr.vec_ok = (reinterpret_cast<uintptr_t>(o.out) % 16 == 0) && (o.ldo % 8 == 0) ? 1 : 0;
+    pr.gqa_head_dim = o.gqa_head_dim;
+    pr.gqa_group = o.gqa_group;
+    pr.out = o.out;
+    pr.ldo = o.ldo;
+    P.probs.push_back(pr);
+    tiles[g] = (o.N + 127) / 128;
+    nkb[g] = pr.nkb;
+    ubase[g + 1] = ubase[g] + static_cast<int64_t>(tiles[g]) * nkb[g];
+  }
+  const int64_t U = ubase[n_ops];
+  // contributors of every tile: (cta, index of the segment in that CTA's list)
+  std::vector<std::vector<std::pair<int, int>>> contrib;
+  std::vector<int64_t> tile_base(n_ops + 1, 0);
+  for (int g = 0; g < n_ops; ++g) tile_base[g + 1] = tile_base[g] + tiles[g];
+  contrib.resize(tile_base[n_ops]);
+  for (int c = 0; c < P.G; ++c) {
+    int64_t u = U * c / P.G;
+    const int64_t u1 = U * (c + 1) / P.G;
+    while (u < u1) {
+      int g = 0;
+      while (ubase[g + 1] <= u) ++g;
+      const int64_t lu = u - ubase[g];
+      const int tile = static_cast<int>(lu / nkb[g]);
+      const int kb0 = static_cast<int>(lu % nkb[g]);
+      const int64_t tile_end = ubase[g] + static_cast<int64_t>(tile + 1) * nkb[g];
+      const int64_t e = std::min(u1, tile_end);
+      PSeg sg;
+      memset(&sg, 0, sizeof(sg));
+      sg.phase = phase;
+      sg.prob = prob0 + g;
+      sg.tile = tile;
+      sg.kb0 = kb0;
+      sg.kb1 = kb0 + static_cast<int>(e - u);
+      sg.nc = 1;
+      contrib[tile_base[g] + tile].push_back({c, static_cast<int>(P.per_cta[c].size())});
+      P.per_cta[c].push_back(sg);
+      u = e;
+    }
+  }
+  int slots = 0;
+  for (auto& list : contrib) {
+    const int nc = static_cast<int>(list.size());
+    if (nc <= 1) continue;
+    const int ctr = P.n_ctr++;
+    for (int j = 0; j < nc; ++j) {
+      PSeg& sg = P.per_cta[list[j].first][list[j].second];
+      sg.j = j;
+      sg.nc = nc;
+      sg.slot = slots;
+      sg.ctr = ctr;
+    }
+    slots += nc;
+  }
+  P.max_slots = std::max(P.max_slots, slots);
+}
+
+// Builds the phase program of one decode step over the stack's fixed buffers.
+void build_plan(const lr_stack_desc* st, Plan& P) {
+  P.G = persist_grid();
+  P.M = static_cast<int>(st->cap);
+  P.nt = pick_nt(st->cap);
+  P.per_cta.assign(P.G, {});
+  const int d = st->layers[0].d_model;
+  uint8_t* ws = static_cast<uint8_t*>(st->scratch);
+  float* h = st->h;
+  add_glue(P, PH_GATHER, d, st->pool_in, nullptr, h, st->xbuf, 0.f);
+  for (int l = 0; l < st->n_layers; ++l) {
+    const lr_block_desc* b = &st->layers[l];
+    const BlockLayout L = block_layout(st->cap, b);
+    const lr_factor* f = b->f;
+    const int dff = b->d_ff;
+    void* t[7];
+    for (int i = 0; i < 7; ++i) t[i] = ws + L.t[i];
+    add_glue(P, PH_RMSNORM, d, h, nullptr, ws + L.n1, nullptr, b->eps);
+    GemmOp down[3], up[3];
+    void* outs[3] = {ws + L.q, ws + L.k, ws + L.v};
+    for (int i = 0; i < 3; ++i) {
+      down[i] = make_op(f[i].At, f[i].r, d, ws + L.n1, d, d, EPI_STORE_BF16, t[i], f[i].r);
+      up[i] = make_op(f[i].Bt, f[i].d_out, f[i].r, t[i], f[i].r, f[i].r, EPI_STORE_BF16, outs[i],
+                      f[i].d_out);
+    }
+    add_gemm(P, down, 3);
+    add_gemm(P, up, 3);
+    const int dq = b->n_heads * b->head_dim, dkv = b->n_kv_heads * b->head_dim;
+    GemmOp od = make_op(f[LR_O].At, f[LR_O].r, dq, ws + L.v, dkv, dkv, EPI_STORE_BF16, t[LR_O],
+                        f[LR_O].r);
+    if (b->n_heads != b->n_kv_heads) {
+      od.gqa_head_dim = b->head_dim;
+      od.gqa_group = b->n_heads / b->n_kv_heads;
+    }
+    GemmOp ou = make_op(f[LR_O].Bt, d, f[LR_O].r, t[LR_O], f[LR_O].r, f[LR_O].r, EPI_ADD_F32, h, d);
+    add_gemm(P, &od, 1);
+    add_gemm(P, &ou, 1);
+    add_glue(P, PH_RMSNORM, d, h, nullptr, ws + L.n2, nullptr, b->eps);
+    GemmOp gd[2], gu[2];
+    void* gouts[2] = {ws + L.g, ws + L.u};
+    for (int i = 0; i < 2; ++i) {
+      const lr_factor& fi = f[LR_GATE + i];
+      gd[i] = make_op(fi.At, fi.r, d, ws + L.n2, d, d, EPI_STORE_BF16, t[LR_GATE + i], fi.r);
+      gu[i] = make_op(fi.Bt, dff, fi.r, t[LR_GATE + i], fi.r, fi.r, EPI_STORE_BF16, gouts[i], dff);
+    }
+    add_gemm(P, gd, 2);
+    add_gemm(P, gu, 2);
+    add_glue(P, PH_SILU, dff, ws + L.g, ws + L.u, ws + L.a, nullptr, 0.f);
+    const lr_factor& fd = f[LR_DOWN];
+    GemmOp dd = make_op(fd.At, fd.r, dff, ws + L.a, dff, dff, EPI_STORE_BF16, t[LR_DOWN], fd.r);
+    GemmOp du = make_op(fd.Bt, d, fd.r, t[LR_DOWN], fd.r, fd.r, EPI_ADD_F32, h, d);
+    add_gemm(P, &dd, 1);
+    add_gemm(P, &du, 1);
+  }
+  add_glue(P, PH_SCATTER, d, h, nullptr, st->pool_out, st->ybuf, 0.f);
+
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  P.n_segs = 0;
+  for (auto& v : P.per_cta) P.n_segs += v.size();
+  P.off_maps = take(P.maps.size() * sizeof(CUtensorMap));
+  P.off_phases = take(P.phases.size() * sizeof(PPhase));
+  P.off_probs = take(P.probs.size() * sizeof(PProblem));
+  P.off_segs = take(P.n_segs * sizeof(PSeg));
+  P.off_begin = take((P.G + 1) * sizeof(int32_t));
+  P.off_partials = take(static_cast<size_t>(std::max(P.max_slots, 1)) * P.nt * 128 * sizeof(float));
+  P.off_zero = off;
+  P.zero_bytes = align_up((P.n_ctr + 2) * sizeof(uint32_t));
+  P.total = P.off_zero + P.zero_bytes;
+}
+
+// Encodes the tensor maps and copies the program into the persistent region;
+// returns the kernel's parameters.  Ordered on stream `s`, and complete on
+// return.
+lr_status upload_plan(const lr_stack_desc* st, Plan& P, cudaStream_t s, PersistParams* out) {
+  uint8_t* region = static_cast<uint8_t*>(st->scratch) + block_region_bytes(st);
+  std::vector<uint8_t> host(P.off_partials, 0);
+  CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(host.data() + P.off_maps);
+  for (size_t i = 0; i < P.maps.size(); ++i) {
+    const MapReq& m = P.maps[i];
+    lr_status r = encode_map_bf16(&maps[i], m.ptr, m.rows, m.cols, m.ld, m.box_rows);
+    if (r != LR_OK) return r;
+  }
+  memcpy(host.data() + P.off_phases, P.phases.data(), P.phases.size() * sizeof(PPhase));
+  memcpy(host.data() + P.off_probs, P.probs.data(), P.probs.size() * sizeof(PProblem));
+  PSeg* segs = reinterpret_cast<PSeg*>(host.data() + P.off_segs);
+  int32_t* begin = reinterpret_cast<int32_t*>(host.data() + P.off_begin);
+  size_t k = 0;
+  for (int c = 0; c < P.G; ++c) {
+    begin[c] = static_cast<int32_t>(k);
+    for (const PSeg& sg : P.per_cta[c]) segs[k++] = sg;
+  }
+  begin[P.G] = static_cast<int32_t>(k);
+  cudaError_t e = cudaMemcpyAsync(region, host.data(), host.size(), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stack: upload program");
+  PersistParams& p = *out;
+  memset(&p, 0, sizeof(p));
+  p.M = P.M;
+  p.G = P.G;
+  p.n_phases = static_cast<int32_t>(P.phases.size());
+  p.pf_ahead = persist_prefetch_tiles();
+  p.phases = reinterpret_cast<const PPhase*>(region + P.off_phases);
+  p.probs = reinterpret_cast<const PProblem*>(region + P.off_probs);
+  p.segs = reinterpret_cast<const PSeg*>(region + P.off_segs);
+  p.seg_begin = reinterpret_cast<const int32_t*>(region + P.off_begin);
+  p.maps = reinterpret_cast<const CUtensorMap*>(region + P.off_maps);
+  p.partials = reinterpret_cast<float*>(region + P.off_partials);
+  p.counters = reinterpret_cast<uint32_t*>(region + P.off_zero);
+  p.gbar = p.counters + P.n_ctr;
+  p.abort_flag = reinterpret_cast<int32_t*>(p.gbar + 1);
+  p.status = st->dev_status;
+  p.remap = st->remap;
+  p.n_active = st->n_active;
+  p.pool_rows = st->pool_rows;
+  return LR_OK;
+}
+
 lr_status check_stack(const lr_stack_desc* st) {
   if (st == nullptr) return invalid("stack: null descriptor");
   if (st->n_layers < 0 || (st->n_layers > 0 && st->layers == nullptr))
     return invalid("stack: bad layer array");
   if (st->n_layers == 0) return invalid("stack: no layers");
   if (st->cap <= 0 || st->cap > kDecodeMaxRows * 64) return invalid("stack: bad cap");
+  if (st->mode != LR_STACK_AUTO && st->mode != LR_STACK_LAYERED && st->mode != LR_STACK_PERSISTENT)
+    return invalid("stack: bad mode");
+  if (st->mode == LR_STACK_PERSISTENT && st->cap > persist_max_rows())
+    return invalid("stack: the persistent step takes at most %d rows", persist_max_rows());
   if (!st->pool_in || !st->pool_out || !st->remap || !st->n_active || !st->xbuf || !st->h ||
       !st->ybuf || !st->scratch)
     return invalid("stack: null pointer");
@@ -311,18 +581,18 @@ lr_status check_stack(const lr_stack_desc* st) {
     return invalid("stack: misaligned buffer");
   if (st->pool_rows <= 0) return invalid("stack: empty pool");
   const int d = st->layers[0].d_model;
-  size_t need = 0;
   for (int l = 0; l < st->n_layers; ++l) {
     lr_status s2 = check_block(&st->layers[l]);
     if (s2 != LR_OK) return s2;
     if (st->layers[l].d_model != d) return invalid("stack: layers disagree on d_model");
-    need = std::max(need, block_layout(st->cap, &st->layers[l]).total);
   }
+  const size_t need = lr_stack_scratch_bytes(st);
   if (st->scratch_bytes < need) return invalid("stack: scratch %zu < %zu bytes", st->scratch_bytes, need);
   return LR_OK;
 }
 
-lr_status enqueue_stack(const lr_stack_desc* st, cudaStream_t s) {
+// One step with one launch per kernel.
+lr_status enqueue_layered(const lr_stack_desc* st, cudaStream_t s) {
   const int d = st->layers[0].d_model;
   const int64_t row_bytes = static_cast<int64_t>(d) * 2;
   lr_status r = launch_gather(st->pool_in, st->pool_rows, row_bytes, st->remap, st->n_active,
@@ -339,6 +609,21 @@ lr_status enqueue_stack(const lr_stack_desc* st, cudaStream_t s) {
   if (r != LR_OK) return r;
   return launch_scatter(st->ybuf, st->remap, st->n_active, st->pool_out, st->pool_rows,
                         row_bytes, st->cap, st->dev_status, s);
+}
+
+// Prepares (program upload, synchronous) and enqueues the persistent step.
+lr_status prepare_persist(const lr_stack_desc* st, cudaStream_t s, PersistParams* p, int* nt,
+                          void** zero_base, size_t* zero_bytes) {
+  lr_status r = ensure_configured();
+  if (r != LR_OK) return r;
+  Plan P;
+  build_plan(st, P);
+  r = upload_plan(st, P, s, p);
+  if (r != LR_OK) return r;
+  *nt = P.nt;
+  *zero_base = static_cast<uint8_t*>(st->scratch) + block_region_bytes(st) + P.off_zero;
+  *zero_bytes = P.zero_bytes;
+  return LR_OK;
 }
 
 }  // namespace
@@ -480,14 +765,38 @@ lr_status remap_build(const int32_t* lengths, int64_t n_seq, const int32_t* bloc
   return LR_OK;
 }
 
+size_t lr_stack_scratch_bytes(const lr_stack_desc* st) {
+  if (st == nullptr || st->layers == nullptr || st->n_layers <= 0 || st->cap <= 0) return 0;
+  size_t n = block_region_bytes(st);
+  if (use_persist(st)) {
+    Plan P;
+    build_plan(st, P);
+    n += P.total;
+  }
+  return n;
+}
+
 lr_status lr_stack_forward(const lr_stack_desc* st, lr_stream s) {
   lr_status r = check_stack(st);
   if (r != LR_OK) return r;
-  return enqueue_stack(st, reinterpret_cast<cudaStream_t>(s));
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+  if (!use_persist(st)) {
+    r = ensure_configured();
+    if (r != LR_OK) return r;
+    return enqueue_layered(st, cs);
+  }
+  PersistParams p;
+  int nt = 0;
+  void* zb = nullptr;
+  size_t zn = 0;
+  r = prepare_persist(st, cs, &p, &nt, &zb, &zn);
+  if (r != LR_OK) return r;
+  return launch_persist(p, nt, zb, zn, cs);
 }
 
 int64_t lr_stack_launch_count(const lr_stack_desc* st) {
   if (st == nullptr || st->layers == nullptr) return 0;
+  if (use_persist(st)) return 1;
   int64_t n = 4;  // gather, widen, narrow, scatter
   for (int l = 0; l < st->n_layers; ++l) n += block_launches(st->cap, &st->layers[l]);
   return n;
@@ -503,18 +812,26 @@ lr_status lr_graph_capture(const lr_stack_desc* st, lr_graph** out) {
   cudaStream_t cs = nullptr;
   cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
   if (e != cudaSuccess) return cuda_fail(e, "graph_capture: stream");
+  PersistParams p;
+  int nt = 0;
+  void* zb = nullptr;
+  size_t zn = 0;
+  const bool persist = use_persist(st);
+  if (persist) r = prepare_persist(st, cs, &p, &nt, &zb, &zn);
   lr_graph* g = new lr_graph();
-  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
-  if (e != cudaSuccess) {
-    r = cuda_fail(e, "graph_capture: begin");
-  } else {
-    lr_status r2 = enqueue_stack(st, cs);
-    e = cudaStreamEndCapture(cs, &g->graph);
-    if (r2 != LR_OK) r = r2;
-    else if (e != cudaSuccess) r = cuda_fail(e, "graph_capture: end");
-    else {
-      e = cudaGraphInstantiate(&g->exec, g->graph, 0);
-      if (e != cudaSuccess) r = cuda_fail(e, "graph_capture: instantiate");
+  if (r == LR_OK) {
+    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) {
+      r = cuda_fail(e, "graph_capture: begin");
+    } else {
+      lr_status r2 = persist ? launch_persist(p, nt, zb, zn, cs) : enqueue_layered(st, cs);
+      e = cudaStreamEndCapture(cs, &g->graph);
+      if (r2 != LR_OK) r = r2;
+      else if (e != cudaSuccess) r = cuda_fail(e, "graph_capture: end");
+      else {
+        e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+        if (e != cudaSuccess) r = cuda_fail(e, "graph_capture: instantiate");
+      }
     }
   }
   cudaStreamDestroy(cs);

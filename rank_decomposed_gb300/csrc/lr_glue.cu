@@ -93,7 +93,11 @@ __global__ void __launch_bounds__(256) scatter_kernel(const uint4* __restrict__ 
   for (int64_t v = threadIdx.x; v < row_vecs; v += blockDim.x) dst[v] = src[v];
 }
 
-// out[m] = bf16(h[m] / sqrt(mean(h[m]^2) + eps)); one CTA per row.
+// out[m] = bf16(h[m] / sqrt(mean(h[m]^2) + eps)); one CTA per row.  Each
+// thread keeps its (up to 8) float4 of the row in registers, so the row is
+// read once and all loads are in flight together.
+constexpr int kNormVec = 8;
+
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float4* __restrict__ h,
                                                       uint2* __restrict__ out, int d4, float eps) {
   pdl_launch_dependents();
@@ -101,11 +105,15 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float4* __restrict__
   __shared__ float part[8];
   const int64_t row = blockIdx.x;
   const float4* x = h + row * d4;
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < d4; i += blockDim.x) {
-    const float4 v = x[i];
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  float4 v[kNormVec];
+#pragma unroll
+  for (int j = 0; j < kNormVec; ++j) {
+    const int idx = threadIdx.x + j * 256;
+    v[j] = idx < d4 ? x[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kNormVec; ++j) ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
@@ -115,14 +123,17 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float4* __restrict__
   for (int w = 0; w < 8; ++w) tot += part[w];
   const float inv = 1.0f / sqrtf(tot / static_cast<float>(4 * d4) + eps);
   uint2* y = out + row * d4;
-  for (int i = threadIdx.x; i < d4; i += blockDim.x) {
-    const float4 v = x[i];
-    uint2 w;
-    w.x = static_cast<uint32_t>(f32_to_bf16_rn(v.x * inv)) |
-          (static_cast<uint32_t>(f32_to_bf16_rn(v.y * inv)) << 16);
-    w.y = static_cast<uint32_t>(f32_to_bf16_rn(v.z * inv)) |
-          (static_cast<uint32_t>(f32_to_bf16_rn(v.w * inv)) << 16);
-    y[i] = w;
+#pragma unroll
+  for (int j = 0; j < kNormVec; ++j) {
+    const int idx = threadIdx.x + j * 256;
+    if (idx < d4) {
+      uint2 w;
+      w.x = static_cast<uint32_t>(f32_to_bf16_rn(v[j].x * inv)) |
+            (static_cast<uint32_t>(f32_to_bf16_rn(v[j].y * inv)) << 16);
+      w.y = static_cast<uint32_t>(f32_to_bf16_rn(v[j].z * inv)) |
+            (static_cast<uint32_t>(f32_to_bf16_rn(v[j].w * inv)) << 16);
+      y[idx] = w;
+    }
   }
 }
 

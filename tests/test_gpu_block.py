@@ -63,7 +63,7 @@ def test_block_llama7b_decode64():
     assert_parity(out - h0, ref - h0, "7B block delta")
 
 
-def _make_stack(cfg, n_layers, cap, n_seq, seed=4):
+def _make_stack(cfg, n_layers, cap, n_seq, seed=4, mode=0):
     layers, hosts = zip(*[make_layer(seed, l, cfg) for l in range(n_layers)])
     L, table, total = synth.paged_batch(seed, n_seq, 20, 300, 16)
     pool_rows = total * 16
@@ -79,9 +79,9 @@ def _make_stack(cfg, n_layers, cap, n_seq, seed=4):
         h=torch.zeros(cap, d, dtype=torch.float32, device="cuda"),
         ybuf=torch.zeros(cap, d, dtype=torch.bfloat16, device="cuda"),
         status=torch.zeros(1, dtype=torch.int32, device="cuda"))
-    dev["scratch"] = torch.zeros(lr.Stack.scratch_bytes(cap, layers), dtype=torch.uint8,
+    dev["scratch"] = torch.zeros(lr.Stack.scratch_bytes(cap, layers, mode), dtype=torch.uint8,
                                  device="cuda")
-    stack = lr.Stack(list(layers), **dev)
+    stack = lr.Stack(list(layers), mode=mode, **dev)
     return stack, list(hosts), pool_bits, remap, n_active
 
 
@@ -90,9 +90,10 @@ def _oracle_stack(cfg, hosts, pool_bits, remap, n):
     return oracle.stack_forward(x, hosts, cfg["n_heads"], cfg["n_kv"], cfg["hd"])
 
 
-def test_stack_eager_graph_and_remap():
+@pytest.mark.parametrize("mode", [lr.STACK_AUTO, lr.STACK_PERSISTENT])
+def test_stack_eager_graph_and_remap(mode):
     cfg, cap = SMALL, 16
-    stack, hosts, pool_bits, remap, n = _make_stack(cfg, 3, cap, 12)
+    stack, hosts, pool_bits, remap, n = _make_stack(cfg, 3, cap, 12, mode=mode)
     assert n == 12
     stack.forward()
     torch.cuda.synchronize()
@@ -133,5 +134,43 @@ def test_stack_eager_graph_and_remap():
 
 
 def test_stack_launch_count():
-    stack, *_ = _make_stack(SMALL, 2, 8, 6)
+    stack, *_ = _make_stack(SMALL, 2, 8, 6, mode=lr.STACK_LAYERED)
     assert stack.launch_count() == 4 + 2 * 11
+    stack, *_ = _make_stack(SMALL, 2, 8, 6, mode=lr.STACK_PERSISTENT)
+    assert stack.launch_count() == 1
+
+
+@pytest.mark.parametrize("cap,n_seq", [(1, 1), (16, 16), (100, 90), (256, 256)])
+def test_persistent_stack_caps(cap, n_seq):
+    """Every token tile width of the persistent kernel (16, 32->64, 128, 256) against the oracle."""
+    cfg = SMALL
+    stack, hosts, pool_bits, remap, n = _make_stack(cfg, 2, cap, n_seq, seed=5,
+                                                    mode=lr.STACK_PERSISTENT)
+    stack.capture()
+    stack.replay()
+    torch.cuda.synchronize()
+    assert int(stack.status.item()) == 0
+    ref = _oracle_stack(cfg, hosts, pool_bits, remap, n)
+    assert_parity(stack.h[:n].cpu().numpy(), ref, "persistent cap=%d" % cap)
+    stack.destroy()
+
+
+def test_persistent_matches_layered_llama7b():
+    """Two 7B-shaped layers, 64 rows: persistent and layered steps against the oracle and each other."""
+    cfg, cap = LLAMA7B, 64
+    outs = []
+    for mode in (lr.STACK_PERSISTENT, lr.STACK_LAYERED):
+        stack, hosts, pool_bits, remap, n = _make_stack(cfg, 2, cap, 64, seed=6, mode=mode)
+        stack.capture()
+        for _ in range(2):
+            stack.replay()
+        torch.cuda.synchronize()
+        assert int(stack.status.item()) == 0
+        outs.append(stack.h.clone())
+        stack.destroy()
+    ref = _oracle_stack(cfg, hosts, pool_bits, remap, n)
+    x0 = oracle.widen_bf16(pool_bits[remap[:n]])
+    for h in outs:
+        out = h[:n].cpu().numpy().astype(np.float64)
+        assert_parity(out - x0, ref - x0, "7B stack delta")
+    assert_parity(outs[0].cpu().numpy(), outs[1].cpu().numpy(), "persistent vs layered")
