@@ -27,9 +27,22 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
-D, DFF, NH, NKV, HD = 4096, 11008, 32, 32, 128
 RHO = 0.4
 BLOCK_ROWS = 16
+
+
+class Model:
+    """LLaMA-shaped block dimensions of a decomposed stack."""
+
+    def __init__(self, name, d, dff, nh, nkv, hd, layers):
+        self.name, self.d, self.dff, self.nh, self.nkv, self.hd, self.layers = name, d, dff, nh, nkv, hd, layers
+
+
+MODELS = {
+    "llama7b": Model("llama7b", 4096, 11008, 32, 32, 128, 32),
+    "llama70b": Model("llama70b", 8192, 28672, 64, 8, 128, 80),   # GQA, 8 kv heads
+}
+LLAMA7B = MODELS["llama7b"]
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -41,8 +54,9 @@ def rank_for(d_in, d_out, rho):
     return int(64 * max((exact / 64 + Fraction(1, 2)).__floor__(), 1))
 
 
-def shapes(rho=RHO):
-    io = [(D, NH * HD), (D, NKV * HD), (D, NKV * HD), (NH * HD, D), (D, DFF), (D, DFF), (DFF, D)]
+def shapes(rho=RHO, m=LLAMA7B):
+    d, dff, dq, dkv = m.d, m.dff, m.nh * m.hd, m.nkv * m.hd
+    io = [(d, dq), (d, dkv), (d, dkv), (dq, d), (d, dff), (d, dff), (dff, d)]
     return [(a, b, rank_for(a, b, rho)) for a, b in io]
 
 
@@ -51,8 +65,8 @@ def linear_bytes(M, d_in, d_out, r):
     return 2 * r * (d_in + d_out) + 2 * M * (d_in + d_out)
 
 
-def step_bytes(M, n_layers, rho=RHO):
-    return n_layers * sum(linear_bytes(M, a, b, r) for a, b, r in shapes(rho))
+def step_bytes(M, n_layers, rho=RHO, m=LLAMA7B):
+    return n_layers * sum(linear_bytes(M, a, b, r) for a, b, r in shapes(rho, m))
 
 
 def load_peaks():
@@ -124,15 +138,18 @@ class Clocks:
 
 # -------------------------------------------------------------- our arm
 class Workload:
-    def __init__(self, torch, lr, M, n_layers, seed=0, rho=RHO, n_seq=None, mode=0):
+    def __init__(self, torch, lr, M, n_layers, seed=0, rho=RHO, n_seq=None, mode=0, model=LLAMA7B,
+                 layers=None):
         self.torch, self.lr = torch, lr
-        self.M, self.n_layers, self.rho = M, n_layers, rho
+        self.M, self.n_layers, self.rho, self.model = M, n_layers, rho, model
+        m = model
+        D = m.d
         dev = "cuda"
-        self.layers = []
+        self.layers = [] if layers is None else layers
         cs_cache = {}
-        for l in range(n_layers):
+        for l in range(0 if layers is not None else n_layers):
             fs = []
-            for p, (a, b, r) in enumerate(shapes(rho)):
+            for p, (a, b, r) in enumerate(shapes(rho, m)):
                 sa, sg = synth.factor_stds(a, r)
                 At = torch.empty((r, a), dtype=torch.bfloat16, device=dev)
                 Bt = torch.empty((b, r), dtype=torch.bfloat16, device=dev)
@@ -142,7 +159,7 @@ class Workload:
                 synth.fill_bf16_normal_device(Bt.data_ptr(), b, r, seed, synth.make_tag(l, p, synth.KIND_B), sg,
                                               cs_cache[r].data_ptr())
                 fs.append(lr.FactorPair(At, Bt))
-            self.layers.append(lr.Block(D, DFF, NH, NKV, HD, fs))
+            self.layers.append(lr.Block(m.d, m.dff, m.nh, m.nkv, m.hd, fs))
         torch.cuda.synchronize()
         n_seq = M if n_seq is None else n_seq
         self.lengths, self.table, pool_rows = batch(seed, n_seq, M)
@@ -162,6 +179,7 @@ class Workload:
 
     def free(self):
         self.stack.destroy()
+        self.stack = None
 
 
 def time_graph(torch, stack, steps, warmup, clocks=None, barrier=None):
@@ -206,7 +224,7 @@ def time_e2e(torch, lr, w, steps, warmup):
     cap = w.M
     remap_h = torch.empty(cap, dtype=torch.int32, pin_memory=True)
     nact_h = torch.empty(1, dtype=torch.int32, pin_memory=True)
-    out_h = torch.empty((cap, D), dtype=torch.bfloat16, pin_memory=True)
+    out_h = torch.empty((cap, w.model.d), dtype=torch.bfloat16, pin_memory=True)
     rh, nh = remap_h.numpy(), nact_h.numpy()
 
     def one():
@@ -236,7 +254,7 @@ def time_linears(torch, lr, w, reps=3):
     pairs then bracket only the kernels.  Returns (sum of algorithmic bytes,
     sum of times in s, launches, per-projection GB/s).
     """
-    M = w.M
+    M, DFF = w.M, w.model.dff
     x = torch.empty((M, DFF), dtype=torch.bfloat16, device="cuda")
     synth.fill_bf16_normal_device(x.data_ptr(), M, DFF, 1, synth.make_tag(0, 0, synth.KIND_X), 1.0)
     y = torch.empty((M, DFF), dtype=torch.bfloat16, device="cuda")
@@ -270,15 +288,16 @@ def time_linears(torch, lr, w, reps=3):
     return float(sum(nbytes)), float(tot), 2 * n, {k: round(v[0] / v[1] / 1e9, 1) for k, v in per_proj.items()}
 
 
-def time_prefill(torch, lr, M=16384, rhos=(0.2, 0.4, 0.6), reps=3):
-    """Config-2 prefill: the 7 projections of one 7B layer at M rows, per rank sweep."""
+def time_prefill(torch, lr, M=16384, rhos=(0.2, 0.4, 0.6), reps=3, m=LLAMA7B):
+    """Prefill: the 7 projections of one layer at M rows, per rank sweep."""
     out = {}
+    DFF = m.dff
     x = torch.empty((M, DFF), dtype=torch.bfloat16, device="cuda")
     synth.fill_bf16_normal_device(x.data_ptr(), M, DFF, 2, synth.make_tag(0, 0, synth.KIND_X), 1.0)
     y = torch.empty((M, DFF), dtype=torch.bfloat16, device="cuda")
     for rho in rhos:
         fs = []
-        for p, (a, b, r) in enumerate(shapes(rho)):
+        for p, (a, b, r) in enumerate(shapes(rho, m)):
             sa, sg = synth.factor_stds(a, r)
             At = torch.empty((r, a), dtype=torch.bfloat16, device="cuda")
             Bt = torch.empty((b, r), dtype=torch.bfloat16, device="cuda")
@@ -302,16 +321,17 @@ def time_prefill(torch, lr, M=16384, rhos=(0.2, 0.4, 0.6), reps=3):
             t = e0.elapsed_time(e1) * 1e-3
             best = t if best is None else min(best, t)
         out[str(rho)] = {"ranks": [f.r for f in fs], "ms_per_layer": round(best * 1e3, 3),
-                         "tokens_per_s_32_layers": round(M / (best * 32), 1),
+                         "tokens_per_s_%d_layers" % m.layers: round(M / (best * m.layers), 1),
                          "tflops": round(flops / best / 1e12, 1)}
         del fs, ws
         torch.cuda.empty_cache()
     return out
 
 
-def oracle_sample(M, layers_sample, seed=0, rho=RHO):
+def oracle_sample(M, layers_sample, seed=0, rho=RHO, m=LLAMA7B):
     """Time the fp64 oracle on M rows through `layers_sample` layers (factor generation untimed)."""
     import oracle
+    D, NH, NKV, HD = m.d, m.nh, m.nkv, m.hd
     L, table, pool_rows = batch(seed, M, M)
     remap, n, _ = oracle.remap_build(L, table, BLOCK_ROWS, 1, M)
     # the active rows of the pool, regenerated element-exactly from their stream offsets
@@ -321,7 +341,7 @@ def oracle_sample(M, layers_sample, seed=0, rho=RHO):
     total = 0.0
     for l in range(layers_sample):
         fac = {}
-        for p, (a, b, r) in enumerate(shapes(rho)):
+        for p, (a, b, r) in enumerate(shapes(rho, m)):
             At, Bt = synth.factor_pair(seed, l, p, a, b, r)
             fac[synth.PROJ_NAMES[p]] = oracle.factor_from_stored(At, Bt)
         t0 = time.perf_counter()
@@ -349,20 +369,26 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="llama7b", choices=sorted(MODELS))
     ap.add_argument("--M", type=int, default=64)
-    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--layers", type=int, default=0, help="0: the model's layer count")
     ap.add_argument("--no-extras", action="store_true", help="skip the M sweep, eager and prefill legs")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
+    model = MODELS[args.config]
+    if args.layers <= 0:
+        args.layers = model.layers
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    workload = ("LLaMA-7B-shaped 32-layer decomposed stack (rho=0.4; q/k/v/o r=1216, gate/up/down "
-                "r=1792), decode M=%d rows compacted by remap from a paged pool, CUDA-graph replay"
-                % args.M) if args.layers == 32 else "LLaMA-7B-shaped %d-layer stack, M=%d" % (args.layers, args.M)
+    rk = shapes(RHO, model)
+    workload = ("%s-shaped %d-layer decomposed stack (rho=0.4; ranks q %d, k/v %d, o %d, gate/up/down %d), "
+                "decode M=%d rows compacted by remap from a paged pool, CUDA-graph replay"
+                % ("LLaMA-7B" if model.name == "llama7b" else "LLaMA-70B (GQA)", args.layers, rk[0][2], rk[1][2],
+                   rk[3][2], rk[4][2], args.M))
 
     if args.impl == "reference":
         if rank != 0:
@@ -382,7 +408,7 @@ def main():
         torch.cuda.set_device(0)
     barrier = (lambda: dist.barrier()) if dist else None
 
-    w = Workload(torch, lr, args.M, args.layers, seed=rank)
+    w = Workload(torch, lr, args.M, args.layers, seed=rank, model=model)
     w.stack.capture()
     clocks = Clocks(torch.cuda.current_device() if world == 1 else local)
     ms, ck = time_graph(torch, w.stack, args.steps, args.warmup, clocks, barrier)
@@ -402,13 +428,13 @@ def main():
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload, "model": "llama-7b-shaped factorized stack (random factors)",
+        "config": {"workload": workload, "model": "%s-shaped factorized stack (random factors)" % model.name,
                    "global_batch": tokens, "seq_len": 1, "rows_per_gpu": args.M,
                    "layers": args.layers, "rho": RHO, "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs larger than L2: %.2f GB of factors streamed per step" % (step_bytes(args.M, args.layers) / 1e9),
+                   "l2": "inputs larger than L2: %.2f GB of factors streamed per step" % (step_bytes(args.M, args.layers, m=model) / 1e9),
                    "remap_runs": w.n_runs},
         "clocks": ck, "gpu_launches": launches,
-        "step_hbm_gbs": round(step_bytes(args.M, args.layers) / (ms * 1e-3) / 1e9, 1),
+        "step_hbm_gbs": round(step_bytes(args.M, args.layers, m=model) / (ms * 1e-3) / 1e9, 1),
     }
     if rank == 0:
         e2e_s, bi, bo = time_e2e(torch, lr, w, max(5, args.steps // 2), 3)
@@ -439,28 +465,34 @@ def main():
             pers_ms, _ = time_graph(torch, w.stack, 10, 3)
             cmp["persistent_graph_ms"] = round(pers_ms, 4)
             line["graph_vs_eager"] = cmp
+        layers = w.layers
         w.free()
         del w
         torch.cuda.empty_cache()
         if not args.no_extras:
             sweep = {}
-            for M in (1, 8, 32, 64):
-                ww = Workload(torch, lr, M, args.layers, seed=0)
+            for M in ((1, 8, 32, 64) if model.name == "llama7b" else (1, 16, 64, 256)):
+                ww = Workload(torch, lr, M, args.layers, seed=0, model=model, layers=layers)
                 ww.stack.capture()
                 t, _ = time_graph(torch, ww.stack, max(10, args.steps // 2), 3)
                 sweep[str(M)] = {"ms_per_step": round(t, 4), "tokens_per_s": round(M / (t * 1e-3), 1),
-                                 "step_hbm_gbs": round(step_bytes(M, args.layers) / (t * 1e-3) / 1e9, 1)}
+                                 "step_hbm_gbs": round(step_bytes(M, args.layers, m=model) / (t * 1e-3) / 1e9, 1)}
                 ww.free()
                 del ww
                 torch.cuda.empty_cache()
             line["decode_sweep"] = sweep
-            pre = time_prefill(torch, lr)
+            del layers
+            torch.cuda.empty_cache()
+            if model.name == "llama7b":
+                pre = time_prefill(torch, lr)
+            else:
+                pre = time_prefill(torch, lr, M=8 * 4096, rhos=(0.4,), m=model)
             for v in pre.values():
                 v["frac_of_bf16_peak"] = round(v["tflops"] / tf, 4)
             line["prefill"] = pre
         if not args.no_cpu:
             sample_layers = min(8, args.layers)
-            tcpu, n = oracle_sample(args.M, sample_layers)
+            tcpu, n = oracle_sample(args.M, sample_layers, m=model)
             v = n / (tcpu * args.layers / sample_layers)
             line["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": cpu_threads(),
                                     "kind": "oracle",
@@ -475,11 +507,12 @@ def main():
 def run_reference(args, workload):
     """The oracle as it stands, on the host cores: each step is 1 layer of the stack for M rows."""
     import oracle  # noqa: F401
+    model = MODELS[args.config]
     for _ in range(args.warmup):
-        oracle_sample(args.M, 1)
+        oracle_sample(args.M, 1, m=model)
     tot, n = 0.0, 0
     for _ in range(args.steps):
-        t, n = oracle_sample(args.M, 1)
+        t, n = oracle_sample(args.M, 1, m=model)
         tot += t
     per_layer = tot / args.steps
     value = n / (per_layer * args.layers)

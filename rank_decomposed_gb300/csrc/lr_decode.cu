@@ -64,12 +64,14 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) 
   return remote;
 }
 
+// Remote shared-memory load.  No memory clobber: the loads are ordered after
+// the cluster barrier that precedes them (which is a compiler barrier), and
+// leaving them free lets the compiler keep many in flight.
 __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
+               : "r"(addr));
   return v;
 }
 
@@ -110,8 +112,53 @@ __device__ __forceinline__ void store_out4(const DecodeProblem& P, int m, int n,
   }
 }
 
+// Sum tokens [t0, t1) x 128 rows of the tile over the S partial tiles of the
+// cluster, in rank order, four rows at a time; CH chunks per iteration keep
+// CH * S remote loads in flight.
+template <int CH, int MAXS>
+__device__ __forceinline__ void reduce_slice(const DecodeProblem& P, const float* ptile, int S,
+                                             int t0, int t1, int n0, int et) {
+  const int nchunks = (t1 - t0) * (kTileN / 4);
+  const uint32_t pbase = smem_u32(ptile);
+  uint32_t rbase[MAXS];
+#pragma unroll
+  for (int s2 = 0; s2 < MAXS; ++s2)
+    rbase[s2] = s2 < S ? cluster_addr(pbase, static_cast<uint32_t>(s2)) : 0u;
+  for (int c = et; c < nchunks; c += 128 * CH) {
+    float4 v[CH][MAXS];
+#pragma unroll
+    for (int h = 0; h < CH; ++h) {
+      const int cc = c + h * 128;
+      if (cc < nchunks) {
+        const uint32_t off = static_cast<uint32_t>(((t0 + cc / 32) * kTileN + (cc % 32) * 4) * 4);
+#pragma unroll
+        for (int s2 = 0; s2 < MAXS; ++s2)
+          if (s2 < S) v[h][s2] = ld_cluster_f32x4(rbase[s2] + off);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < CH; ++h) {
+      const int cc = c + h * 128;
+      if (cc >= nchunks) break;
+      const int tok = t0 + cc / 32;
+      const int row = (cc % 32) * 4;
+      if (n0 + row >= P.N) continue;  // N is a multiple of 64: 4 rows all in or all out
+      float4 acc = v[h][0];
+#pragma unroll
+      for (int s2 = 1; s2 < MAXS; ++s2)
+        if (s2 < S) {
+          acc.x += v[h][s2].x;
+          acc.y += v[h][s2].y;
+          acc.z += v[h][s2].z;
+          acc.w += v[h][s2].w;
+        }
+      store_out4(P, tok, n0 + row, acc);
+    }
+  }
+}
+
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ DecodeMaps maps) {
   constexpr int kStages = DecodeCfg<NT>::kStages;
   constexpr int kABytes = NT * kBK * 2;
@@ -227,9 +274,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Every MMA issued by this thread completes before TMEM is released.
       mbar_wait(&accum_bar, 0, nullptr);
     }
+  } else if (S == 1) {
+    // Epilogue, whole K in this CTA: TMEM lanes 32*(warp%4) .. +31 hold weight
+    // rows, the columns are tokens; store straight to the output.
+    const int q = warp & 3;
+    const int n = n0 + q * 32 + lane;
+    bool ok = mbar_wait(&accum_bar, 0, &abort_sh);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      pdl_wait();  // outputs (e.g. the residual stream) belong to earlier kernels
+#pragma unroll 1
+      for (int c = 0; c < NT / 16; ++c) {
+        if (c * 16 >= p.M) break;
+        uint32_t r[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, r);
+        tmem_ld_wait();
+        if (n < P.N) {
+          const int nt = p.M - c * 16 < 16 ? p.M - c * 16 : 16;
+          if (P.epi == EPI_ADD_F32) {
+            float* o = static_cast<float*>(P.out) + n;
+            float hv[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j < nt) hv[j] = o[static_cast<int64_t>(c * 16 + j) * P.ldo];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j < nt) o[static_cast<int64_t>(c * 16 + j) * P.ldo] = hv[j] + __uint_as_float(r[j]);
+          } else if (P.epi == EPI_STORE_F32) {
+            float* o = static_cast<float*>(P.out) + n;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j < nt) o[static_cast<int64_t>(c * 16 + j) * P.ldo] = __uint_as_float(r[j]);
+          } else {
+            uint16_t* o = static_cast<uint16_t*>(P.out) + n;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j < nt) o[static_cast<int64_t>(c * 16 + j) * P.ldo] = f32_to_bf16_rn(__uint_as_float(r[j]));
+          }
+        }
+      }
+    } else if (lane == 0) {
+      abort_sh = 1;
+      report_status(p.status, LR_ERR_TIMEOUT);
+    }
   } else {
-    // Epilogue warps: TMEM lanes 32*(warp%4) .. +31 hold weight rows; the
-    // columns are tokens.  Copy the valid tokens into this CTA's partial tile.
+    // Epilogue warps, K split over the cluster: copy the valid tokens of the
+    // TMEM accumulator into this CTA's partial tile.
     const int q = warp & 3;
     const int row = q * 32 + lane;
     bool ok = mbar_wait(&accum_bar, 0, &abort_sh);
@@ -254,46 +345,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (S > 1) {
   __syncwarp();
   cluster_sync_all();  // every partial tile of the cluster is in shared memory
 
   if (warp >= 2) {
     // Reduce this CTA's share of the tile -- tokens [t0, t1) x 128 rows -- over
-    // the S partial tiles of the cluster, in rank order, four rows at a time.
+    // the S partial tiles of the cluster.
     pdl_wait();  // outputs (e.g. the residual stream) belong to earlier kernels
     const int et = threadIdx.x - 64;
     const int t0 = split * p.M / S;
     const int t1 = (split + 1) * p.M / S;
-    const int nchunks = (t1 - t0) * (kTileN / 4);
-    const uint32_t pbase = smem_u32(ptile);
-    uint32_t rbase[kMaxCluster];
-#pragma unroll
-    for (int s2 = 0; s2 < kMaxCluster; ++s2)
-      rbase[s2] = s2 < S ? cluster_addr(pbase, static_cast<uint32_t>(s2)) : 0u;
-    for (int c = et; c < nchunks; c += 128) {
-      const int tok = t0 + c / (kTileN / 4);
-      const int row = (c % (kTileN / 4)) * 4;
-      if (n0 + row >= P.N) continue;  // N is a multiple of 64: the 4 rows are all in or all out
-      const uint32_t off = static_cast<uint32_t>((tok * kTileN + row) * 4);
-      float4 v[kMaxCluster];
-#pragma unroll
-      for (int s2 = 0; s2 < kMaxCluster; ++s2)
-        if (s2 < S) v[s2] = ld_cluster_f32x4(rbase[s2] + off);
-      float4 acc = v[0];
-#pragma unroll
-      for (int s2 = 1; s2 < kMaxCluster; ++s2)
-        if (s2 < S) {
-          acc.x += v[s2].x;
-          acc.y += v[s2].y;
-          acc.z += v[s2].z;
-          acc.w += v[s2].w;
-        }
-      store_out4(P, tok, n0 + row, acc);
-    }
+    if (S <= 8)
+      reduce_slice<2, 8>(P, ptile, S, t0, t1, n0, et);
+    else
+      reduce_slice<1, kMaxCluster>(P, ptile, S, t0, t1, n0, et);
   }
 
   __syncwarp();
   cluster_sync_all();  // no CTA leaves while others read its shared memory
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
