@@ -297,7 +297,7 @@ lr_status enqueue_block(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws
 }
 
 int64_t block_launches(int64_t M, const lr_block_desc*) {
-  // rmsnorm x2, silu_mul, and the GEMM launches.
+  // rmsnorm x2, silu_mul, and the GEMM launches (grouped for decode sizes).
   if (M <= kDecodeMaxRows) return 3 + 8;
   return 3 + 14;
 }
@@ -595,16 +595,25 @@ lr_status check_stack(const lr_stack_desc* st) {
 lr_status enqueue_layered(const lr_stack_desc* st, cudaStream_t s) {
   const int d = st->layers[0].d_model;
   const int64_t row_bytes = static_cast<int64_t>(d) * 2;
-  lr_status r = launch_gather(st->pool_in, st->pool_rows, row_bytes, st->remap, st->n_active,
-                              st->xbuf, st->cap, st->dev_status, s);
-  if (r != LR_OK) return r;
-  r = launch_widen(st->xbuf, st->h, st->cap * d, s);
+  uint8_t* ws = static_cast<uint8_t*>(st->scratch);
+  lr_status r;
+  const bool decode = st->cap <= kDecodeMaxRows;
+  if (decode) {
+    r = launch_gather_rows(st->pool_in, st->pool_rows, d, st->remap, st->n_active, st->xbuf, st->h,
+                           st->cap, st->dev_status, s);
+  } else {
+    r = launch_gather(st->pool_in, st->pool_rows, row_bytes, st->remap, st->n_active, st->xbuf,
+                      st->cap, st->dev_status, s);
+    if (r == LR_OK) r = launch_widen(st->xbuf, st->h, st->cap * d, s);
+  }
   if (r != LR_OK) return r;
   for (int l = 0; l < st->n_layers; ++l) {
-    r = enqueue_block(st->h, st->cap, &st->layers[l], static_cast<uint8_t*>(st->scratch),
-                      st->dev_status, s);
+    r = enqueue_block(st->h, st->cap, &st->layers[l], ws, st->dev_status, s);
     if (r != LR_OK) return r;
   }
+  if (decode)
+    return launch_scatter_rows(st->h, st->ybuf, st->remap, st->n_active, st->pool_out,
+                               st->pool_rows, d, st->cap, st->dev_status, s);
   r = launch_narrow(st->h, st->ybuf, st->cap * d, s);
   if (r != LR_OK) return r;
   return launch_scatter(st->ybuf, st->remap, st->n_active, st->pool_out, st->pool_rows,
@@ -797,7 +806,8 @@ lr_status lr_stack_forward(const lr_stack_desc* st, lr_stream s) {
 int64_t lr_stack_launch_count(const lr_stack_desc* st) {
   if (st == nullptr || st->layers == nullptr) return 0;
   if (use_persist(st)) return 1;
-  int64_t n = 4;  // gather, widen, narrow, scatter
+  const bool decode = st->cap <= kDecodeMaxRows;
+  int64_t n = decode ? 2 : 4;  // gather(+widen), (narrow+)scatter
   for (int l = 0; l < st->n_layers; ++l) n += block_launches(st->cap, &st->layers[l]);
   return n;
 }

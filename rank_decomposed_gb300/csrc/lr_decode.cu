@@ -228,9 +228,6 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
         mbar_arrive_expect_tx(&full_bar[i], kStageBytes);
         tma_load_2d(w_smem + i * kWBytes, mw, &full_bar[i], (kb0 + i) * kBK, n0, pol_w);
       }
-      // The rest of this CTA's weight range goes to L2 now, while the
-      // previous kernel may still be running.
-      for (int i = npre; i < nk; ++i) tma_prefetch_l2_2d(mw, (kb0 + i) * kBK, n0);
       pdl_wait();
       for (int i = 0; i < npre; ++i)
         tma_load_2d(a_smem + i * kABytes, ma, &full_bar[i], act_col(P, kb0 + i), 0, pol_a);

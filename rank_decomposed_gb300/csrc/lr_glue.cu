@@ -196,6 +196,65 @@ __global__ void __launch_bounds__(256) narrow_kernel(const float4* __restrict__ 
   }
 }
 
+// One stack row: xbuf[i] = pool[remap[i]] (zero past n_active), h[i] = widen.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ pool, int64_t pool_rows,
+                                                          int d8, const int32_t* __restrict__ remap,
+                                                          const int32_t* __restrict__ n_active,
+                                                          uint4* __restrict__ xbuf, float4* __restrict__ h,
+                                                          int64_t cap, int32_t* status) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t i = blockIdx.x;
+  const int n = clamp_active(n_active, cap);
+  const uint4* src = nullptr;
+  if (i < n) {
+    const int64_t j = remap[i];
+    if (j >= 0 && j < pool_rows)
+      src = pool + j * d8;
+    else if (threadIdx.x == 0)
+      report_status(status, LR_ERR_REMAP_RANGE);
+  }
+  for (int v = threadIdx.x; v < d8; v += 256) {
+    const uint4 w = src != nullptr ? src[v] : make_uint4(0, 0, 0, 0);
+    xbuf[i * d8 + v] = w;
+    h[(i * d8 + v) * 2] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                                      __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+    h[(i * d8 + v) * 2 + 1] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u),
+                                          __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
+  }
+}
+
+// One stack row: ybuf[i] = bf16(h[i]); pool[remap[i]] = ybuf[i] for i < n_active.
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const float4* __restrict__ h, int d8,
+                                                           uint4* __restrict__ ybuf,
+                                                           const int32_t* __restrict__ remap,
+                                                           const int32_t* __restrict__ n_active,
+                                                           uint4* __restrict__ pool, int64_t pool_rows,
+                                                           int64_t cap, int32_t* status) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t i = blockIdx.x;
+  const int n = clamp_active(n_active, cap);
+  uint4* dst = nullptr;
+  if (i < n) {
+    const int64_t j = remap[i];
+    if (j >= 0 && j < pool_rows)
+      dst = pool + j * d8;
+    else if (threadIdx.x == 0)
+      report_status(status, LR_ERR_REMAP_RANGE);
+  }
+  for (int v = threadIdx.x; v < d8; v += 256) {
+    const float4 a = h[(i * d8 + v) * 2], b = h[(i * d8 + v) * 2 + 1];
+    uint4 w;
+    w.x = static_cast<uint32_t>(f32_to_bf16_rn(a.x)) | (static_cast<uint32_t>(f32_to_bf16_rn(a.y)) << 16);
+    w.y = static_cast<uint32_t>(f32_to_bf16_rn(a.z)) | (static_cast<uint32_t>(f32_to_bf16_rn(a.w)) << 16);
+    w.z = static_cast<uint32_t>(f32_to_bf16_rn(b.x)) | (static_cast<uint32_t>(f32_to_bf16_rn(b.y)) << 16);
+    w.w = static_cast<uint32_t>(f32_to_bf16_rn(b.z)) | (static_cast<uint32_t>(f32_to_bf16_rn(b.w)) << 16);
+    ybuf[i * d8 + v] = w;
+    if (dst != nullptr) dst[v] = w;
+  }
+}
+
 int elementwise_grid(int64_t n_vec) {
   const int64_t per = 256;
   int64_t blocks = (n_vec + per - 1) / per;
@@ -214,6 +273,24 @@ lr_status launch_gather(const void* pool, int64_t pool_rows, int64_t row_bytes,
   return launch(gather_kernel, dim3(static_cast<unsigned>(cap)), dim3(256), s, "gather",
                 static_cast<const uint4*>(pool), pool_rows, row_bytes / 16, remap, n_active,
                 static_cast<uint4*>(buf), cap, status);
+}
+
+lr_status launch_gather_rows(const void* pool, int64_t pool_rows, int d, const int32_t* remap,
+                             const int32_t* n_active, void* xbuf, float* h, int64_t cap,
+                             int32_t* status, cudaStream_t s) {
+  if (cap == 0) return LR_OK;
+  return launch(gather_rows_kernel, dim3(static_cast<unsigned>(cap)), dim3(256), s, "gather_rows",
+                static_cast<const uint4*>(pool), pool_rows, d / 8, remap, n_active,
+                static_cast<uint4*>(xbuf), reinterpret_cast<float4*>(h), cap, status);
+}
+
+lr_status launch_scatter_rows(const float* h, void* ybuf, const int32_t* remap,
+                              const int32_t* n_active, void* pool, int64_t pool_rows, int d,
+                              int64_t cap, int32_t* status, cudaStream_t s) {
+  if (cap == 0) return LR_OK;
+  return launch(scatter_rows_kernel, dim3(static_cast<unsigned>(cap)), dim3(256), s, "scatter_rows",
+                reinterpret_cast<const float4*>(h), d / 8, static_cast<uint4*>(ybuf), remap, n_active,
+                static_cast<uint4*>(pool), pool_rows, cap, status);
 }
 
 lr_status launch_scatter(const void* buf, const int32_t* remap, const int32_t* n_active,

@@ -163,6 +163,13 @@ lr_status launch_silu_mul(const void* g, const void* u, void* out, int64_t M, in
                           cudaStream_t s);
 lr_status launch_widen(const void* in_bf16, float* out, int64_t n, cudaStream_t s);
 lr_status launch_narrow(const float* in, void* out_bf16, int64_t n, cudaStream_t s);
+// Stack glue, one CTA per row: gather + widen, and narrow + scatter.
+lr_status launch_gather_rows(const void* pool, int64_t pool_rows, int d, const int32_t* remap,
+                             const int32_t* n_active, void* xbuf, float* h, int64_t cap,
+                             int32_t* status, cudaStream_t s);
+lr_status launch_scatter_rows(const float* h, void* ybuf, const int32_t* remap,
+                              const int32_t* n_active, void* pool, int64_t pool_rows, int d,
+                              int64_t cap, int32_t* status, cudaStream_t s);
 lr_status launch_gather(const void* pool, int64_t pool_rows, int64_t row_bytes,
                         const int32_t* remap, const int32_t* n_active, void* buf, int64_t cap,
                         int32_t* status, cudaStream_t s);
