@@ -375,11 +375,16 @@ int env_int(const char* name, int dflt) {
   return (v && *v) ? atoi(v) : dflt;
 }
 
-// Pick the number of K splits (= cluster size) of a launch: minimise the
-// per-SM share of weight tiles plus a per-wave overhead, in units of one
-// 128 x 64 weight tile.
-int choose_splits(const GemmOp* ops, int n_ops, int slots) {
+// Pick the number of K splits (= cluster size) of a launch: minimise, in units
+// of one 128 x 64 weight tile, the per-SM share of weight tiles, plus a fixed
+// cost per wave of CTAs (launch, pipeline fill, epilogue) and the cluster
+// reduction, which reads S partial tiles of M tokens.  The two weights were
+// fitted by sweeping them on the 7B-shaped decode step (M = 1..64).
+// LR_DECODE_SPLITS forces a split count (a measurement switch).
+int choose_splits(const GemmOp* ops, int n_ops, int slots, int M) {
   static const int forced = env_int("LR_DECODE_SPLITS", 0);
+  constexpr double overhead = 16.0;
+  constexpr double red = 0.5;
   int tiles = 0, min_nkb = 1 << 30;
   for (int g = 0; g < n_ops; ++g) {
     tiles += (ops[g].N + kTileN - 1) / kTileN;
@@ -388,7 +393,6 @@ int choose_splits(const GemmOp* ops, int n_ops, int slots) {
   const int smax = std::min(kMaxCluster, min_nkb);
   if (forced > 0) return std::min(forced, smax);
   const int sms = num_sms();
-  const double overhead = 4.0;
   int best = 1;
   double best_cost = 1e30;
   for (int S = 1; S <= smax; ++S) {
@@ -397,7 +401,8 @@ int choose_splits(const GemmOp* ops, int n_ops, int slots) {
     for (int g = 0; g < n_ops; ++g) umax = std::max(umax, (ops[g].K / kBK + S - 1) / S);
     const double per_sm = std::ceil(static_cast<double>(C) / sms) * umax;
     const double waves = std::ceil(static_cast<double>(C) / (static_cast<double>(sms) * slots));
-    const double cost = per_sm + overhead * waves;
+    // the cluster reduction reads S partial tiles of M tokens per tile
+    const double cost = per_sm + overhead * waves + (S > 1 ? red * S * M / 64.0 : 0.0);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = S;
@@ -426,7 +431,7 @@ lr_status launch_nt(int M, const GemmOp* ops, int n_ops, int32_t* status, cudaSt
   prm.M = M;
   prm.n_problems = n_ops;
   prm.status = status;
-  const int S = choose_splits(ops, n_ops, DecodeCfg<NT>::kSlots);
+  const int S = choose_splits(ops, n_ops, DecodeCfg<NT>::kSlots, M);
   prm.splits = S;
   int items = 0;
   for (int g = 0; g < n_ops; ++g) {
