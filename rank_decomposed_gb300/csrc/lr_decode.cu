@@ -215,7 +215,9 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
   pdl_launch_dependents();
 
   if (warp == 0) {
-    if (lane == 0) {
+    // (With the fault-injection hook set the producer issues nothing: the MMA
+    // thread's bounded wait runs out and the launch reports LR_ERR_TIMEOUT.)
+    if (lane == 0 && !p.stall_producer) {
       const CUtensorMap* mw = &maps.w[g];
       const CUtensorMap* ma = &maps.a[g];
       prefetch_tensormap(mw);
@@ -433,6 +435,8 @@ lr_status launch_nt(int M, const GemmOp* ops, int n_ops, int32_t* status, cudaSt
   prm.status = status;
   const int S = choose_splits(ops, n_ops, DecodeCfg<NT>::kSlots, M);
   prm.splits = S;
+  // Fault injection for the timeout path (tests only): read at every launch.
+  prm.stall_producer = env_int("LR_TEST_STALL_PRODUCER", 0) != 0 ? 1 : 0;
   int items = 0;
   for (int g = 0; g < n_ops; ++g) {
     const GemmOp& o = ops[g];

@@ -63,7 +63,7 @@ struct DecodeParams {
   int32_t M;            // valid rows (tokens), 1..256
   int32_t n_problems;
   int32_t splits;       // K splits per tile == cluster size
-  int32_t pad_;
+  int32_t stall_producer;  // fault-injection hook: the TMA producer issues nothing
   int32_t* status;
   DecodeProblem prob[kMaxGroup];
 };
