@@ -69,6 +69,31 @@ def step_bytes(M, n_layers, rho=RHO, m=LLAMA7B):
     return n_layers * sum(linear_bytes(M, a, b, r) for a, b, r in shapes(rho, m))
 
 
+def decode_traffic():
+    """Per-launch DRAM traffic of the decode kernel from profiles/, or None.
+
+    The profile records a hash of the kernel source it was taken on; a
+    changed kernel makes the figure stale, and then None is reported.
+    """
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "decode_kernel_traffic.txt")
+    src = os.path.join(ROOT, "rank_decomposed_gb300", "csrc", "lr_decode.cu")
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    kv = {}
+    for line in open(prof):
+        if "=" in line and not line.startswith("#"):
+            k, v = line.strip().split("=", 1)
+            kv[k.strip()] = v.strip()
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if kv.get("source_sha256") != digest:
+        return None
+    try:
+        return float(kv["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -374,6 +399,9 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="0: the model's layer count")
     ap.add_argument("--no-extras", action="store_true", help="skip the M sweep, eager and prefill legs")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--only", choices=["roofline", "prefill"],
+                    help="run one leg alone (for profiling): the event-timed decode linears, or "
+                         "the prefill projections at rho=0.4")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -408,7 +436,18 @@ def main():
         torch.cuda.set_device(0)
     barrier = (lambda: dist.barrier()) if dist else None
 
+    if args.only == "prefill":
+        M = 16384 if model.name == "llama7b" else 8 * 4096
+        print(json.dumps({"leg": "prefill", "config": model.name, "M": M,
+                          "result": time_prefill(torch, lr, M=M, rhos=(0.4,), m=model, reps=2)}))
+        return
     w = Workload(torch, lr, args.M, args.layers, seed=rank, model=model)
+    if args.only == "roofline":
+        nbytes, tsum, nl, per_proj = time_linears(torch, lr, w, reps=1)
+        print(json.dumps({"leg": "roofline", "config": model.name, "M": args.M, "layers": args.layers,
+                          "launches": nl, "algorithmic_bytes_per_launch": nbytes / nl,
+                          "achieved_gbs": nbytes / tsum / 1e9}))
+        return
     w.stack.capture()
     clocks = Clocks(torch.cuda.current_device() if world == 1 else local)
     ms, ck = time_graph(torch, w.stack, args.steps, args.warmup, clocks, barrier)
@@ -444,8 +483,9 @@ def main():
                        "path": "host remap_build + pinned H2D of remap/n_active + graph replay + D2H of the step's rows"}
         nbytes, tsum, nl, per_proj = time_linears(torch, lr, w)
         achieved = nbytes / tsum / 1e9
+        traffic = decode_traffic() if model.name == "llama7b" and args.M == 64 else None
         line["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                            "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": peak_kind,
+                            "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": peak_kind,
                             "kernel": "decode_kernel (tcgen05 swap-AB), down+up launches of every linear",
                             "launches_timed": nl, "avg_launch_us": round(tsum / nl * 1e6, 2),
                             "algorithmic_bytes_per_launch": round(nbytes / nl),
