@@ -483,6 +483,17 @@ def main():
         ms = float(t.item())
     if int(w.stack.status.item()) != 0:
         raise SystemExit("device status %d" % int(w.stack.status.item()))
+    # The same graph serves any batch that fits: only the remap contents and
+    # n_active change (a real step writes them before each replay).
+    n_active_check = {}
+    for n in sorted({args.M, max(1, (args.M * 37) // 64), 1}, reverse=True):
+        w.stack.n_active.fill_(n)
+        t_n, _ = time_graph(torch, w.stack, 5, 3)
+        n_active_check[str(n)] = round(t_n, 4)
+    w.stack.n_active.fill_(w.n_active)
+    torch.cuda.synchronize()
+    if int(w.stack.status.item()) != 0:
+        raise SystemExit("device status %d after n_active replays" % int(w.stack.status.item()))
     tokens = args.M * world
     value = tokens / (ms * 1e-3)
     launches = w.stack.launch_count() * args.steps
@@ -498,7 +509,7 @@ def main():
                    "layers": args.layers, "rho": RHO, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2: %.2f GB of factors streamed per step" % (step_bytes(args.M, args.layers, m=model) / 1e9),
                    "remap_runs": w.n_runs},
-        "clocks": ck, "gpu_launches": launches,
+        "clocks": ck, "gpu_launches": launches, "graph_ms_by_n_active": n_active_check,
         "step_hbm_gbs": round(step_bytes(args.M, args.layers, m=model) / (ms * 1e-3) / 1e9, 1),
     }
     if rank == 0:

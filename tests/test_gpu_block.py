@@ -63,6 +63,27 @@ def test_block_llama7b_decode64():
     assert_parity(out - h0, ref - h0, "7B block delta")
 
 
+LLAMA70B = dict(d=8192, d_ff=28672, n_heads=64, n_kv=8, hd=128,
+                ranks=(2432, 576, 576, 2432, 3840, 3840, 3840))
+
+
+@pytest.mark.parametrize("M", [16, 64])
+def test_block_llama70b_gqa_decode(M):
+    """One 70B-shaped block (GQA, 8 kv heads) in decode against the oracle."""
+    cfg = LLAMA70B
+    blk, host = make_layer(0, 3, cfg)
+    bits, h0 = _h_input(1, M, cfg["d"])
+    h = torch.from_numpy(h0.astype(np.float32)).cuda()
+    scratch = torch.zeros(lr.block_scratch_bytes(M, blk), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr.block_forward(h, blk, scratch, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = oracle.block_forward(h0, host, cfg["n_heads"], cfg["n_kv"], cfg["hd"])
+    out = h.cpu().numpy().astype(np.float64)
+    assert_parity(out - h0, ref - h0, "70B block delta M=%d" % M)
+
+
 def _make_stack(cfg, n_layers, cap, n_seq, seed=4, mode=0):
     layers, hosts = zip(*[make_layer(seed, l, cfg) for l in range(n_layers)])
     L, table, total = synth.paged_batch(seed, n_seq, 20, 300, 16)
