@@ -412,6 +412,23 @@ def cpu_threads():
     return os.cpu_count()
 
 
+def aggregate(dist, ms, tokens):
+    """Whole-job step time and tokens over the ranks of a replica run.
+
+    Every rank runs its own batch (no collective on the data path); the job's
+    step takes as long as the slowest rank, and the job's tokens are the sum.
+    """
+    if dist is None:
+        return float(ms), float(tokens)
+    import torch
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=dev)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(n.item())
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -477,10 +494,7 @@ def main():
     w.stack.capture()
     clocks = Clocks(torch.cuda.current_device() if world == 1 else local)
     ms, ck = time_graph(torch, w.stack, args.steps, args.warmup, clocks, barrier)
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, tokens = aggregate(dist, ms, args.M)
     if int(w.stack.status.item()) != 0:
         raise SystemExit("device status %d" % int(w.stack.status.item()))
     # The same graph serves any batch that fits: only the remap contents and
@@ -494,7 +508,6 @@ def main():
     torch.cuda.synchronize()
     if int(w.stack.status.item()) != 0:
         raise SystemExit("device status %d after n_active replays" % int(w.stack.status.item()))
-    tokens = args.M * world
     value = tokens / (ms * 1e-3)
     launches = w.stack.launch_count() * args.steps
 
@@ -505,7 +518,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload, "model": "%s-shaped factorized stack (random factors)" % model.name,
-                   "global_batch": tokens, "seq_len": 1, "rows_per_gpu": args.M,
+                   "global_batch": int(tokens), "seq_len": 1, "rows_per_gpu": args.M,
                    "layers": args.layers, "rho": RHO, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2: %.2f GB of factors streamed per step" % (step_bytes(args.M, args.layers, m=model) / 1e9),
                    "remap_runs": w.n_runs},
