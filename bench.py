@@ -378,6 +378,50 @@ def time_prefill(torch, lr, M=16384, rhos=(0.2, 0.4, 0.6), reps=3, m=LLAMA7B):
     return out
 
 
+def time_kv_reconstruct(torch, lr, m=LLAMA7B, n_seq=64, reps=5):
+    """Low-rank KV reconstruction of a whole decode batch's context.
+
+    Every position of 64 sequences (lengths U{128..4096}) is listed by
+    remap_build, its k latent (r columns) compacted into a fixed buffer, and
+    multiplied by B_k in one fixed-size GEMM, as the pages' graph-replay stage.
+    """
+    d_kv = m.nkv * m.hd
+    r = rank_for(m.d, d_kv, RHO)
+    L, table, pool_rows = batch(7, n_seq, n_seq)
+    cap = int(L.sum())
+    remap, n, runs = lr.remap_build(L, table, BLOCK_ROWS, 0, cap)
+    pool = torch.empty((pool_rows, r), dtype=torch.bfloat16, device="cuda")
+    synth.fill_bf16_normal_device(pool.data_ptr(), pool_rows, r, 7, synth.make_tag(0, 1, synth.KIND_POOL), 1.0)
+    _, sg = synth.factor_stds(m.d, r)
+    Bt = torch.empty((d_kv, r), dtype=torch.bfloat16, device="cuda")
+    cs = torch.from_numpy(synth.sigma_scale(r)).cuda()
+    synth.fill_bf16_normal_device(Bt.data_ptr(), d_kv, r, 7, synth.make_tag(0, synth.PROJ_K, synth.KIND_B), sg,
+                                  cs.data_ptr())
+    buf = torch.empty((cap, r), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((cap, d_kv), dtype=torch.bfloat16, device="cuda")
+    d_remap = torch.from_numpy(remap).cuda()
+    d_n = torch.tensor([n], dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr.kv_reconstruct(pool, d_remap, d_n, buf, Bt, out, st)
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        lr.kv_reconstruct(pool, d_remap, d_n, buf, Bt, out, st)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) * 1e-3
+        best = t if best is None else min(best, t)
+    if int(st.item()) != 0:
+        raise SystemExit("kv_reconstruct status %d" % int(st.item()))
+    flops = 2.0 * cap * r * d_kv
+    nbytes = 2.0 * cap * r * 2 + 2.0 * cap * d_kv + 2.0 * d_kv * r   # gather r/w, out, Bt
+    return {"rows": cap, "r": r, "d_kv": d_kv, "remap_runs": runs, "ms": round(best * 1e3, 4),
+            "rows_per_s": round(cap / best, 1), "tflops": round(flops / best / 1e12, 1),
+            "gbs": round(nbytes / best / 1e9, 1)}
+
+
 def oracle_sample(M, layers_sample, seed=0, rho=RHO, m=LLAMA7B):
     """Time the fp64 oracle on M rows through `layers_sample` layers (factor generation untimed)."""
     import oracle
@@ -585,6 +629,7 @@ def main():
             for v in pre.values():
                 v["frac_of_bf16_peak"] = round(v["tflops"] / tf, 4)
             line["prefill"] = pre
+            line["kv_reconstruct"] = time_kv_reconstruct(torch, lr, m=model)
         if not args.no_cpu:
             sample_layers = min(8, args.layers)
             tcpu, n = oracle_sample(args.M, sample_layers, m=model)

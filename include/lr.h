@@ -196,6 +196,27 @@ lr_status remap_build(const int32_t* lengths, int64_t n_seq, const int32_t* bloc
                       int32_t* remap_out, int32_t* n_active_out, int32_t* n_runs_out);
 
 /* ---------------------------------------------------------------------------
+ * lr_kv_reconstruct: the reconstruction of a low-rank KV cache under a static
+ * graph (English page section 2.C: scattered latent rows are listed by a
+ * remap table, copied into a contiguous buffer, and "the contiguous buffer is
+ * multiplied by the upward projection matrices to reconstruct the KV cache"
+ * in one large fixed-size GEMM; the latent KV grows with the context, English
+ * page section 1).
+ *   latent_buf[i][:] = latent_pool[remap[i]][:] for i < *n_active, zero rows
+ *   otherwise (as remap_compact), then out = latent_buf Bt^T, i.e.
+ *   out[i][n] = sum_j latent_buf[i][j] * B_r[j][n].
+ *   latent_pool: device bf16 [pool_rows][r]; latent_buf: device bf16 [cap][r];
+ *   Bt: device bf16 [d_kv][r] (the up factor transposed); out: device bf16
+ *   [cap][d_kv].  r and d_kv positive multiples of 64, pointers 16-byte
+ *   aligned.  Rows past *n_active come out zero.  cap and every pointer are
+ *   fixed, so the two launches can be captured once and replayed per step.
+ *   Out-of-range remap entries give zero rows and LR_ERR_REMAP_RANGE. */
+lr_status lr_kv_reconstruct(const void* latent_pool, int64_t pool_rows, int32_t r,
+                            const int32_t* remap, const int32_t* n_active, int64_t cap,
+                            void* latent_buf, const void* Bt, int32_t d_kv, void* out,
+                            int32_t* dev_status, lr_stream s);
+
+/* ---------------------------------------------------------------------------
  * A decode step of a layer stack over fixed buffers (English page section 2.C:
  * addresses and launch parameters stay fixed while the logical batch changes):
  *   xbuf = remap_compact(pool_in); h = widen(xbuf); for each layer:

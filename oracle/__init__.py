@@ -215,3 +215,14 @@ def remap_scatter(buf: np.ndarray, remap, n_active: int, pool: np.ndarray):
         else:
             bad = True
     return out, bad
+
+
+def kv_reconstruct(latent_pool: np.ndarray, remap, n_active: int, cap: int, B: np.ndarray):
+    """Low-rank KV reconstruction over a compacted buffer (English page, section 2.C).
+
+    The listed latent rows are copied into a [cap, r] buffer (zero past
+    n_active) and multiplied by the up factor B [r, d_kv]: rows of K (or V).
+    fp64; returns (buffer, reconstructed rows, out-of-range flag).
+    """
+    buf, bad = remap_gather(latent_pool, remap, n_active, cap)
+    return buf, np.asarray(buf, dtype=np.float64) @ np.asarray(B, dtype=np.float64), bad

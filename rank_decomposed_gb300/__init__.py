@@ -78,6 +78,7 @@ def _load():
         "remap_compact": (i32, [vp, i64, i64, vp, vp, vp, i64, vp, vp]),
         "remap_scatter": (i32, [vp, vp, vp, vp, i64, i64, i64, vp, vp]),
         "remap_build": (i32, [vp, i64, vp, i32, i32, i32, i64, vp, vp, vp]),
+        "lr_kv_reconstruct": (i32, [vp, i64, i32, vp, vp, i64, vp, vp, i32, vp, vp, vp]),
         "lr_stack_forward": (i32, [P(StackDesc), vp]),
         "lr_graph_capture": (i32, [P(StackDesc), P(vp)]),
         "lr_graph_replay": (i32, [vp, vp]),
@@ -267,6 +268,23 @@ def remap_build(lengths, block_table, block_rows: int, tail_rows: int, cap: int)
                          tail_rows, cap, out.ctypes.data, ctypes.byref(na), ctypes.byref(nr))
     _check("remap_build", st)
     return out, na.value, nr.value
+
+
+def kv_reconstruct(latent_pool, remap, n_active, latent_buf, Bt, out, status, stream=None):
+    """Compact the listed latent rows into latent_buf, then out = latent_buf Bt^T (bf16)."""
+    _bf16(latent_pool, "latent_pool")
+    _bf16(latent_buf, "latent_buf")
+    _bf16(Bt, "Bt")
+    _bf16(out, "out")
+    r = latent_pool.shape[1]
+    if latent_buf.shape[1] != r or Bt.shape[1] != r or out.shape[1] != Bt.shape[0] \
+            or out.shape[0] != latent_buf.shape[0]:
+        raise ValueError("kv_reconstruct: inconsistent shapes")
+    st = lib.lr_kv_reconstruct(latent_pool.data_ptr(), latent_pool.shape[0], r, remap.data_ptr(),
+                               n_active.data_ptr(), latent_buf.shape[0], latent_buf.data_ptr(),
+                               Bt.data_ptr(), Bt.shape[0], out.data_ptr(), _ptr(status),
+                               _stream(stream))
+    _check("lr_kv_reconstruct", st)
 
 
 # ---------------------------------------------------------------- stack

@@ -736,6 +736,29 @@ lr_status remap_scatter(const void* buf, const int32_t* remap, const int32_t* n_
                         reinterpret_cast<cudaStream_t>(s));
 }
 
+lr_status lr_kv_reconstruct(const void* latent_pool, int64_t pool_rows, int32_t r,
+                            const int32_t* remap, const int32_t* n_active, int64_t cap,
+                            void* latent_buf, const void* Bt, int32_t d_kv, void* out,
+                            int32_t* dev_status, lr_stream s) {
+  if (r <= 0 || d_kv <= 0 || cap < 0 || pool_rows < 0) return invalid("kv_reconstruct: bad sizes");
+  if (r % 64 || d_kv % 64) {
+    set_error("kv_reconstruct: r=%d and d_kv=%d must be multiples of 64", r, d_kv);
+    return LR_ERR_UNSUPPORTED;
+  }
+  if (cap == 0) return LR_OK;
+  if (cap > 0x7FFFFFFF) return invalid("kv_reconstruct: cap too large");
+  if (!latent_pool || !remap || !n_active || !latent_buf || !Bt || !out)
+    return invalid("kv_reconstruct: null pointer");
+  if (!aligned16(latent_pool) || !aligned16(latent_buf) || !aligned16(Bt) || !aligned16(out))
+    return invalid("kv_reconstruct: buffers must be 16-byte aligned");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+  lr_status st = launch_gather(latent_pool, pool_rows, static_cast<int64_t>(r) * 2, remap,
+                               n_active, latent_buf, cap, dev_status, cs);
+  if (st != LR_OK) return st;
+  GemmOp up = make_op(Bt, d_kv, r, latent_buf, r, r, EPI_STORE_BF16, out, d_kv);
+  return run_ops(cap, &up, 1, dev_status, cs);
+}
+
 lr_status remap_build(const int32_t* lengths, int64_t n_seq, const int32_t* block_table,
                       int32_t blocks_per_seq, int32_t block_rows, int32_t tail_rows, int64_t cap,
                       int32_t* remap_out, int32_t* n_active_out, int32_t* n_runs_out) {

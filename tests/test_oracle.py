@@ -261,3 +261,20 @@ def test_remap_out_of_range_and_padding():
     assert np.array_equal(buf[0], pool[3])
     assert not np.any(buf[1]) and not np.any(buf[2])   # bad entries give zero rows
     assert not np.any(buf[3:])                         # rows >= n_active are zero
+
+
+# ----------------------------------------------------- KV reconstruction
+def test_kv_reconstruct_identity_and_commutation():
+    """B = I returns the compacted latents; compacting commutes with the row-wise product."""
+    pool_bits = synth.bf16_normal(5, 90, (50, 64))
+    pool = oracle.widen_bf16(pool_bits)
+    remap = np.full(12, -1, np.int32)
+    remap[:9] = synth.permutation(5, 91, 50)[:9]
+    buf, out, bad = oracle.kv_reconstruct(pool, remap, 9, 12, np.eye(64))
+    assert not bad and np.array_equal(out, buf)
+    assert np.array_equal(buf[:9], pool[remap[:9]]) and not np.any(buf[9:])
+    B = _bf16_matrix(5, 92, (64, 128), 0.125)
+    _, out, _ = oracle.kv_reconstruct(pool, remap, 9, 12, B)
+    full = np.einsum("pj,jn->pn", pool, B)          # reconstruct every pool row, then gather
+    assert np.allclose(out[:9], full[remap[:9]], rtol=0, atol=1e-12)
+    assert not np.any(out[9:])
