@@ -84,7 +84,12 @@ enum { LR_Q = 0, LR_K = 1, LR_V = 2, LR_O = 3, LR_GATE = 4, LR_UP = 5, LR_DOWN =
  * q: d_model -> n_heads*head_dim, k/v: d_model -> n_kv_heads*head_dim,
  * o: n_heads*head_dim -> d_model, gate/up: d_model -> d_ff, down: d_ff -> d_model.
  * n_heads must be a multiple of n_kv_heads (MHA, GQA, MQA); head_dim a multiple
- * of 64; d_model at most 8192; RMSNorm has unit gain and the given eps. */
+ * of 64; d_model at most 8192; RMSNorm has unit gain and the given eps.
+ * The MLP is SiLU-GLU or, with mlp = LR_MLP_RELU, a non-GLU ReLU MLP. */
+/* MLP variants (English page section 2.D: GLU and non-GLU MLPs). */
+enum { LR_MLP_SWIGLU = 0, /* h += down(silu(gate(n2)) * up(n2)) (LLaMA) */
+       LR_MLP_RELU = 1    /* h += down(relu(up(n2))), gate unused (OPT) */ };
+
 typedef struct {
   int32_t d_model;
   int32_t d_ff;
@@ -93,6 +98,7 @@ typedef struct {
   int32_t head_dim;
   float eps;
   lr_factor f[7];
+  int32_t mlp;  /* LR_MLP_SWIGLU or LR_MLP_RELU; with LR_MLP_RELU f[LR_GATE] is not read */
 } lr_block_desc;
 
 /* ---------------------------------------------------------------------------
@@ -147,7 +153,8 @@ lr_status lr_linear_forward_noalloc(const void* x, int64_t ldx, void* y, int64_t
  * lr_block_forward: one decomposed block applied in place to the fp32 residual
  * stream h (device fp32 [M][d_model], 16-byte aligned):
  *   n1 = RMSNorm(h); q,k,v = LR(n1); h += LR_o(attn(v));
- *   n2 = RMSNorm(h); h += LR_down(silu(LR_gate(n2)) * LR_up(n2)).
+ *   n2 = RMSNorm(h); h += LR_down(silu(LR_gate(n2)) * LR_up(n2))
+ *   (non-GLU: h += LR_down(relu(LR_up(n2)))).
  * Spanish page section 1 (attention and MLP projections decomposed) and
  * section 2 "Generalizacion"; English page section 2.D (MHA/GQA/MQA, GLU MLP).
  * Linear inputs are rounded to bf16.  scratch: device, at least

@@ -119,13 +119,20 @@ def one_token_attention(v: np.ndarray, n_heads: int, n_kv_heads: int, head_dim: 
     return out
 
 
+def relu(z: np.ndarray) -> np.ndarray:
+    """max(z, 0)."""
+    return np.maximum(np.asarray(z, dtype=np.float64), 0.0)
+
+
 def block_forward(h: np.ndarray, factors, n_heads: int, n_kv_heads: int, head_dim: int,
-                  eps: float = LLAMA_RMS_EPS, return_all: bool = False):
+                  eps: float = LLAMA_RMS_EPS, return_all: bool = False, mlp: str = "swiglu"):
     """One decomposed LLaMA block, attention core replaced by one-token attention.
 
     ``factors`` maps "q","k","v","o","gate","up","down" to (A, B) fp64 pairs.
     n1 = rmsnorm(h); q, k, v = LR(n1); h1 = h + LR_o(attn(v));
     n2 = rmsnorm(h1); h2 = h1 + LR_down(silu(LR_gate(n2)) * LR_up(n2)).
+    With mlp="relu" (a non-GLU MLP, English page section 2.D) the MLP is
+    h2 = h1 + LR_down(relu(LR_up(n2))) and "gate" is not used.
     """
     h = np.asarray(h, dtype=np.float64)
     n1 = rmsnorm(h, eps)
@@ -136,9 +143,13 @@ def block_forward(h: np.ndarray, factors, n_heads: int, n_kv_heads: int, head_di
     _, o = lowrank_linear(attn, *factors["o"])
     h1 = h + o
     n2 = rmsnorm(h1, eps)
-    _, g = lowrank_linear(n2, *factors["gate"])
     _, u = lowrank_linear(n2, *factors["up"])
-    a = silu(g) * u
+    if mlp == "relu":
+        g = None
+        a = relu(u)
+    else:
+        _, g = lowrank_linear(n2, *factors["gate"])
+        a = silu(g) * u
     _, dn = lowrank_linear(a, *factors["down"])
     h2 = h1 + dn
     if return_all:
@@ -148,10 +159,10 @@ def block_forward(h: np.ndarray, factors, n_heads: int, n_kv_heads: int, head_di
 
 
 def stack_forward(h: np.ndarray, layers, n_heads: int, n_kv_heads: int, head_dim: int,
-                  eps: float = LLAMA_RMS_EPS) -> np.ndarray:
+                  eps: float = LLAMA_RMS_EPS, mlp: str = "swiglu") -> np.ndarray:
     """Apply ``block_forward`` for each factor set in ``layers`` in order."""
     for f in layers:
-        h = block_forward(h, f, n_heads, n_kv_heads, head_dim, eps)
+        h = block_forward(h, f, n_heads, n_kv_heads, head_dim, eps, mlp=mlp)
     return h
 
 

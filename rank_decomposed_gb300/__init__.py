@@ -44,7 +44,12 @@ class Factor(ctypes.Structure):
 class BlockDesc(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("n_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("eps", ctypes.c_float), ("f", Factor * 7)]
+                ("head_dim", ctypes.c_int32), ("eps", ctypes.c_float), ("f", Factor * 7),
+                ("mlp", ctypes.c_int32)]
+
+
+MLP_SWIGLU = 0
+MLP_RELU = 1
 
 
 class StackDesc(ctypes.Structure):
@@ -166,14 +171,17 @@ class Block:
     head_dim: int
     factors: list
     eps: float = 1e-6
+    mlp: int = MLP_SWIGLU   # MLP_RELU: non-GLU, factors[4] (gate) may be None
 
     def c(self) -> BlockDesc:
         b = BlockDesc()
         b.d_model, b.d_ff = self.d_model, self.d_ff
         b.n_heads, b.n_kv_heads, b.head_dim = self.n_heads, self.n_kv_heads, self.head_dim
         b.eps = self.eps
+        b.mlp = self.mlp
         for i, f in enumerate(self.factors):
-            b.f[i] = f.c()
+            if f is not None:
+                b.f[i] = f.c()
         return b
 
 

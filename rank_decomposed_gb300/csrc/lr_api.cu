@@ -190,7 +190,10 @@ BlockLayout block_layout(int64_t M, const lr_block_desc* b) {
   };
   const size_t m = static_cast<size_t>(M);
   L.n1 = take(m * b->d_model * 2);
-  for (int i = 0; i < 7; ++i) L.t[i] = take(m * b->f[i].r * 2);
+  for (int i = 0; i < 7; ++i) {
+    const bool unused = (i == LR_GATE && b->mlp == LR_MLP_RELU);
+    L.t[i] = take(unused ? 0 : m * b->f[i].r * 2);
+  }
   L.q = take(m * b->f[LR_Q].d_out * 2);
   L.k = take(m * b->f[LR_K].d_out * 2);
   L.v = take(m * b->f[LR_V].d_out * 2);
@@ -205,7 +208,9 @@ BlockLayout block_layout(int64_t M, const lr_block_desc* b) {
 lr_status check_block(const lr_block_desc* b) {
   if (b == nullptr) return invalid("block: null descriptor");
   static const char* names[7] = {"q", "k", "v", "o", "gate", "up", "down"};
+  if (b->mlp != LR_MLP_SWIGLU && b->mlp != LR_MLP_RELU) return invalid("block: bad mlp variant");
   for (int i = 0; i < 7; ++i) {
+    if (i == LR_GATE && b->mlp == LR_MLP_RELU) continue;  // not read
     lr_status st = check_factor(&b->f[i], names[i]);
     if (st != LR_OK) return st;
   }
@@ -225,7 +230,8 @@ lr_status check_block(const lr_block_desc* b) {
   const int dq = b->n_heads * hd, dkv = b->n_kv_heads * hd;
   const int want[7][2] = {{d, dq}, {d, dkv}, {d, dkv}, {dq, d}, {d, dff}, {d, dff}, {dff, d}};
   for (int i = 0; i < 7; ++i)
-    if (b->f[i].d_in != want[i][0] || b->f[i].d_out != want[i][1])
+    if (!(i == LR_GATE && b->mlp == LR_MLP_RELU) &&
+        (b->f[i].d_in != want[i][0] || b->f[i].d_out != want[i][1]))
       return invalid("block: factor %s is %dx%d, expected %dx%d", names[i], b->f[i].d_in,
                      b->f[i].d_out, want[i][0], want[i][1]);
   return LR_OK;
@@ -273,7 +279,7 @@ lr_status enqueue_block(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws
   }
   // MLP half: n2 = RMSNorm(h); h += LR_down(silu(LR_gate(n2)) * LR_up(n2))
   LR_TRY(launch_rmsnorm(h, n2, M, d, b->eps, s));
-  {
+  if (b->mlp == LR_MLP_SWIGLU) {
     GemmOp down[2], up[2];
     void* outs[2] = {ws + L.g, ws + L.u};
     for (int i = 0; i < 2; ++i) {
@@ -283,8 +289,16 @@ lr_status enqueue_block(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws
     }
     LR_TRY(run_ops(M, down, 2, status, s));
     LR_TRY(run_ops(M, up, 2, status, s));
+    LR_TRY(launch_silu_mul(ws + L.g, ws + L.u, ws + L.a, M, dff, s));
+  } else {
+    // non-GLU: a = relu(LR_up(n2))
+    const lr_factor& fu = f[LR_UP];
+    GemmOp ud = make_op(fu.At, fu.r, d, n2, d, d, EPI_STORE_BF16, t[LR_UP], fu.r);
+    GemmOp uu = make_op(fu.Bt, dff, fu.r, t[LR_UP], fu.r, fu.r, EPI_STORE_BF16, ws + L.u, dff);
+    LR_TRY(run_ops(M, &ud, 1, status, s));
+    LR_TRY(run_ops(M, &uu, 1, status, s));
+    LR_TRY(launch_relu(ws + L.u, ws + L.a, M, dff, s));
   }
-  LR_TRY(launch_silu_mul(ws + L.g, ws + L.u, ws + L.a, M, dff, s));
   {
     const lr_factor& fd = f[LR_DOWN];
     GemmOp dd = make_op(fd.At, fd.r, dff, ws + L.a, dff, dff, EPI_STORE_BF16, t[LR_DOWN], fd.r);
@@ -296,10 +310,10 @@ lr_status enqueue_block(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws
   return LR_OK;
 }
 
-int64_t block_launches(int64_t M, const lr_block_desc*) {
-  // rmsnorm x2, silu_mul, and the GEMM launches (grouped for decode sizes).
+int64_t block_launches(int64_t M, const lr_block_desc* b) {
+  // rmsnorm x2, silu_mul or relu, and the GEMM launches (grouped for decode sizes).
   if (M <= kDecodeMaxRows) return 3 + 8;
-  return 3 + 14;
+  return 3 + (b->mlp == LR_MLP_RELU ? 12 : 14);
 }
 
 // ---------------------------------------------------------------- stack
@@ -573,6 +587,12 @@ lr_status check_stack(const lr_stack_desc* st) {
     return invalid("stack: bad mode");
   if (st->mode == LR_STACK_PERSISTENT && st->cap > persist_max_rows())
     return invalid("stack: the persistent step takes at most %d rows", persist_max_rows());
+  if (st->mode == LR_STACK_PERSISTENT)
+    for (int l = 0; l < st->n_layers; ++l)
+      if (st->layers[l].mlp != LR_MLP_SWIGLU) {
+        set_error("stack: the persistent step runs SiLU-GLU blocks only");
+        return LR_ERR_UNSUPPORTED;
+      }
   if (!st->pool_in || !st->pool_out || !st->remap || !st->n_active || !st->xbuf || !st->h ||
       !st->ybuf || !st->scratch)
     return invalid("stack: null pointer");

@@ -161,6 +161,7 @@ lr_status launch_rmsnorm(const float* h, void* out_bf16, int64_t M, int d, float
                          cudaStream_t s);
 lr_status launch_silu_mul(const void* g, const void* u, void* out, int64_t M, int d,
                           cudaStream_t s);
+lr_status launch_relu(const void* u, void* out, int64_t M, int d, cudaStream_t s);
 lr_status launch_widen(const void* in_bf16, float* out, int64_t n, cudaStream_t s);
 lr_status launch_narrow(const float* in, void* out_bf16, int64_t n, cudaStream_t s);
 // Stack glue, one CTA per row: gather + widen, and narrow + scatter.

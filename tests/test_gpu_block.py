@@ -18,10 +18,14 @@ LLAMA7B = dict(d=4096, d_ff=11008, n_heads=32, n_kv=32, hd=128,
 
 def make_layer(seed, layer, cfg):
     shapes = block_shapes(cfg["d"], cfg["d_ff"], cfg["n_heads"], cfg["n_kv"], cfg["hd"], cfg["ranks"])
-    dev = [dev_factor(seed, layer, p, a, b, r) for p, (a, b, r) in enumerate(shapes)]
-    host = {synth.PROJ_NAMES[p]: host_factor(seed, layer, p, a, b, r)
+    relu = cfg.get("mlp") == "relu"
+    skip = lambda p: relu and p == synth.PROJ_GATE
+    dev = [None if skip(p) else dev_factor(seed, layer, p, a, b, r)
+           for p, (a, b, r) in enumerate(shapes)]
+    host = {synth.PROJ_NAMES[p]: (None if skip(p) else host_factor(seed, layer, p, a, b, r))
             for p, (a, b, r) in enumerate(shapes)}
-    blk = lr.Block(cfg["d"], cfg["d_ff"], cfg["n_heads"], cfg["n_kv"], cfg["hd"], dev)
+    blk = lr.Block(cfg["d"], cfg["d_ff"], cfg["n_heads"], cfg["n_kv"], cfg["hd"], dev,
+                   mlp=lr.MLP_RELU if relu else lr.MLP_SWIGLU)
     return blk, host
 
 
@@ -196,3 +200,53 @@ def test_persistent_matches_layered_llama7b():
         out = h[:n].cpu().numpy().astype(np.float64)
         assert_parity(out - x0, ref - x0, "7B stack delta")
     assert_parity(outs[0].cpu().numpy(), outs[1].cpu().numpy(), "persistent vs layered")
+
+
+OPT_SMALL = dict(d=512, d_ff=2048, n_heads=8, n_kv=8, hd=64, ranks=(128, 128, 128, 128, 64, 192, 192),
+                 mlp="relu")
+MQA_SMALL = dict(d=512, d_ff=1024, n_heads=8, n_kv=1, hd=64, ranks=(128, 64, 64, 128, 192, 192, 192))
+
+
+@pytest.mark.parametrize("cfg_name,M", [("opt", 4), ("opt", 300), ("mqa", 5), ("mqa", 260)])
+def test_block_variants(cfg_name, M):
+    """Non-GLU (ReLU) MLP with MHA, and MQA (one kv head), in decode and prefill sizes."""
+    cfg = OPT_SMALL if cfg_name == "opt" else MQA_SMALL
+    blk, host = make_layer(13, 0, cfg)
+    bits, h0 = _h_input(13, M, cfg["d"])
+    h = torch.from_numpy(h0.astype(np.float32)).cuda()
+    scratch = torch.zeros(lr.block_scratch_bytes(M, blk), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr.block_forward(h, blk, scratch, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = oracle.block_forward(h0, host, cfg["n_heads"], cfg["n_kv"], cfg["hd"],
+                               mlp=cfg.get("mlp", "swiglu"))
+    out = h.cpu().numpy().astype(np.float64)
+    assert_parity(out - h0, ref - h0, "%s block delta M=%d" % (cfg_name, M))
+
+
+def test_stack_with_per_layer_ranks():
+    """Layers of one stack compressed at different ratios (variadic ranks) under graph replay."""
+    cfg0 = dict(SMALL)
+    cfg1 = dict(SMALL, ranks=(64, 64, 64, 64, 64, 64, 64))
+    cfg2 = dict(SMALL, ranks=(256, 128, 128, 256, 320, 320, 320))
+    layers, hosts = zip(*[make_layer(14, l, c) for l, c in enumerate((cfg0, cfg1, cfg2))])
+    cap, d = 16, SMALL["d"]
+    L, table, total = synth.paged_batch(14, 10, 20, 300, 16)
+    pool_bits = synth.bf16_normal(14, synth.make_tag(0, 0, synth.KIND_POOL), (total * 16, d))
+    remap, n, _ = lr.remap_build(L, table, 16, 1, cap)
+    pool = dev_bits(pool_bits)
+    stack = lr.Stack(list(layers), pool, pool.clone(), torch.from_numpy(remap).cuda(),
+                     torch.tensor([n], dtype=torch.int32, device="cuda"),
+                     torch.zeros(cap, d, dtype=torch.bfloat16, device="cuda"),
+                     torch.zeros(cap, d, dtype=torch.float32, device="cuda"),
+                     torch.zeros(cap, d, dtype=torch.bfloat16, device="cuda"),
+                     torch.zeros(lr.Stack.scratch_bytes(cap, layers), dtype=torch.uint8, device="cuda"),
+                     torch.zeros(1, dtype=torch.int32, device="cuda"))
+    stack.capture()
+    stack.replay()
+    torch.cuda.synchronize()
+    assert int(stack.status.item()) == 0
+    ref = _oracle_stack(SMALL, list(hosts), pool_bits, remap, n)
+    assert_parity(stack.h[:n].cpu().numpy(), ref, "variadic-rank stack")
+    stack.destroy()

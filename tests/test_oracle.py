@@ -278,3 +278,18 @@ def test_kv_reconstruct_identity_and_commutation():
     full = np.einsum("pj,jn->pn", pool, B)          # reconstruct every pool row, then gather
     assert np.allclose(out[:9], full[remap[:9]], rtol=0, atol=1e-12)
     assert not np.any(out[9:])
+
+
+def test_block_relu_mlp_path():
+    """Non-GLU MLP with up = I and down = I: h2 = h1 + max(n2, 0); the gate factor is never read."""
+    d = 16
+    h = _bf16_matrix(12, 1, (3, d))
+    f = _zero_factors(d, d, d)
+    f["up"] = (np.eye(d), np.eye(d))
+    f["down"] = (np.eye(d), np.eye(d))
+    f["gate"] = None
+    out = oracle.block_forward(h, f, 2, 2, 8, return_all=True, mlp="relu")
+    n2 = out["n2"]
+    want = out["h1"] + np.where(n2 > 0, n2, 0.0)
+    assert np.allclose(out["h2"], want, rtol=0, atol=1e-15)
+    assert np.array_equal(oracle.relu(np.array([-2.0, -0.0, 0.0, 3.5])), [0.0, 0.0, 0.0, 3.5])
