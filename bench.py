@@ -32,15 +32,17 @@ BLOCK_ROWS = 16
 
 
 class Model:
-    """LLaMA-shaped block dimensions of a decomposed stack."""
+    """Block dimensions of a decomposed stack (mlp: "swiglu" or the non-GLU "relu")."""
 
-    def __init__(self, name, d, dff, nh, nkv, hd, layers):
+    def __init__(self, name, d, dff, nh, nkv, hd, layers, mlp="swiglu"):
         self.name, self.d, self.dff, self.nh, self.nkv, self.hd, self.layers = name, d, dff, nh, nkv, hd, layers
+        self.mlp = mlp
 
 
 MODELS = {
     "llama7b": Model("llama7b", 4096, 11008, 32, 32, 128, 32),
     "llama70b": Model("llama70b", 8192, 28672, 64, 8, 128, 80),   # GQA, 8 kv heads
+    "opt30b": Model("opt30b", 7168, 28672, 56, 56, 128, 48, mlp="relu"),
 }
 LLAMA7B = MODELS["llama7b"]
 FALLBACK_HBM_GBS = 6800.0
@@ -55,9 +57,11 @@ def rank_for(d_in, d_out, rho):
 
 
 def shapes(rho=RHO, m=LLAMA7B):
+    """(d_in, d_out, r) of the 7 projections; None for the gate of a non-GLU MLP."""
     d, dff, dq, dkv = m.d, m.dff, m.nh * m.hd, m.nkv * m.hd
     io = [(d, dq), (d, dkv), (d, dkv), (dq, d), (d, dff), (d, dff), (dff, d)]
-    return [(a, b, rank_for(a, b, rho)) for a, b in io]
+    return [None if (p == 4 and m.mlp == "relu") else (a, b, rank_for(a, b, rho))
+            for p, (a, b) in enumerate(io)]
 
 
 def linear_bytes(M, d_in, d_out, r):
@@ -66,7 +70,7 @@ def linear_bytes(M, d_in, d_out, r):
 
 
 def step_bytes(M, n_layers, rho=RHO, m=LLAMA7B):
-    return n_layers * sum(linear_bytes(M, a, b, r) for a, b, r in shapes(rho, m))
+    return n_layers * sum(linear_bytes(M, *sh) for sh in shapes(rho, m) if sh is not None)
 
 
 def decode_traffic():
@@ -174,7 +178,11 @@ class Workload:
         cs_cache = {}
         for l in range(0 if layers is not None else n_layers):
             fs = []
-            for p, (a, b, r) in enumerate(shapes(rho, m)):
+            for p, sh in enumerate(shapes(rho, m)):
+                if sh is None:
+                    fs.append(None)
+                    continue
+                a, b, r = sh
                 sa, sg = synth.factor_stds(a, r)
                 At = torch.empty((r, a), dtype=torch.bfloat16, device=dev)
                 Bt = torch.empty((b, r), dtype=torch.bfloat16, device=dev)
@@ -184,7 +192,8 @@ class Workload:
                 synth.fill_bf16_normal_device(Bt.data_ptr(), b, r, seed, synth.make_tag(l, p, synth.KIND_B), sg,
                                               cs_cache[r].data_ptr())
                 fs.append(lr.FactorPair(At, Bt))
-            self.layers.append(lr.Block(m.d, m.dff, m.nh, m.nkv, m.hd, fs))
+            self.layers.append(lr.Block(m.d, m.dff, m.nh, m.nkv, m.hd, fs,
+                                        mlp=lr.MLP_RELU if m.mlp == "relu" else lr.MLP_SWIGLU))
         torch.cuda.synchronize()
         n_seq = M if n_seq is None else n_seq
         self.lengths, self.table, pool_rows = batch(seed, n_seq, M)
@@ -287,9 +296,9 @@ def time_linears(torch, lr, w, reps=3):
     x = torch.empty((M, DFF), dtype=torch.bfloat16, device="cuda")
     synth.fill_bf16_normal_device(x.data_ptr(), M, DFF, 1, synth.make_tag(0, 0, synth.KIND_X), 1.0)
     y = torch.empty((M, DFF), dtype=torch.bfloat16, device="cuda")
-    ws = torch.zeros(max(lr.linear_workspace_bytes(M, f) for f in w.layers[0].factors),
+    ws = torch.zeros(max(lr.linear_workspace_bytes(M, f) for f in w.layers[0].factors if f is not None),
                      dtype=torch.uint8, device="cuda")
-    calls = [(p, f) for b in w.layers for p, f in enumerate(b.factors)]
+    calls = [(p, f) for b in w.layers for p, f in enumerate(b.factors) if f is not None]
     n = len(calls)
     nbytes = [linear_bytes(M, f.d_in, f.d_out, f.r) for _, f in calls]
     for p, f in calls[:7]:
@@ -347,7 +356,10 @@ def time_prefill(torch, lr, M=16384, rhos=(0.2, 0.4, 0.6), reps=3, m=LLAMA7B):
     y = torch.empty((M, DFF), dtype=torch.bfloat16, device="cuda")
     for rho in rhos:
         fs = []
-        for p, (a, b, r) in enumerate(shapes(rho, m)):
+        for p, sh in enumerate(shapes(rho, m)):
+            if sh is None:
+                continue
+            a, b, r = sh
             sa, sg = synth.factor_stds(a, r)
             At = torch.empty((r, a), dtype=torch.bfloat16, device="cuda")
             Bt = torch.empty((b, r), dtype=torch.bfloat16, device="cuda")
@@ -435,11 +447,14 @@ def oracle_sample(M, layers_sample, seed=0, rho=RHO, m=LLAMA7B):
     total = 0.0
     for l in range(layers_sample):
         fac = {}
-        for p, (a, b, r) in enumerate(shapes(rho, m)):
-            At, Bt = synth.factor_pair(seed, l, p, a, b, r)
+        for p, sh in enumerate(shapes(rho, m)):
+            if sh is None:
+                fac[synth.PROJ_NAMES[p]] = None
+                continue
+            At, Bt = synth.factor_pair(seed, l, p, *sh)
             fac[synth.PROJ_NAMES[p]] = oracle.factor_from_stored(At, Bt)
         t0 = time.perf_counter()
-        h = oracle.block_forward(h, fac, NH, NKV, HD)
+        h = oracle.block_forward(h, fac, NH, NKV, HD, mlp=m.mlp)
         total += time.perf_counter() - t0
     return total, n
 
@@ -499,10 +514,10 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     rk = shapes(RHO, model)
-    workload = ("%s-shaped %d-layer decomposed stack (rho=0.4; ranks q %d, k/v %d, o %d, gate/up/down %d), "
+    label = {"llama7b": "LLaMA-7B", "llama70b": "LLaMA-70B (GQA)", "opt30b": "OPT-30B (ReLU MLP)"}[model.name]
+    workload = ("%s-shaped %d-layer decomposed stack (rho=0.4; ranks q %d, k/v %d, o %d, mlp %d), "
                 "decode M=%d rows compacted by remap from a paged pool, CUDA-graph replay"
-                % ("LLaMA-7B" if model.name == "llama7b" else "LLaMA-70B (GQA)", args.layers, rk[0][2], rk[1][2],
-                   rk[3][2], rk[4][2], args.M))
+                % (label, args.layers, rk[0][2], rk[1][2], rk[3][2], rk[5][2], args.M))
 
     if args.impl == "reference":
         if rank != 0:
@@ -523,7 +538,7 @@ def main():
     barrier = (lambda: dist.barrier()) if dist else None
 
     if args.only == "prefill":
-        M = 16384 if model.name == "llama7b" else 8 * 4096
+        M = 8 * 4096 if model.name == "llama70b" else 16384
         print(json.dumps({"leg": "prefill", "config": model.name, "M": M,
                           "result": time_prefill(torch, lr, M=M, rhos=(0.4,), m=model, reps=2)}))
         return
@@ -595,14 +610,15 @@ def main():
             eager_ms = time_eager(torch, w.stack, 5, 3)
             cmp = {"graph_ms": round(ms, 4), "eager_ms": round(eager_ms, 4),
                    "launches_per_step": w.stack.launch_count()}
-            w.stack.destroy()
-            w.stack.mode = lr.STACK_PERSISTENT
-            w.stack._desc = None
-            need = lr.Stack.scratch_bytes(args.M, w.layers, lr.STACK_PERSISTENT)
-            w.stack.scratch = torch.zeros(need, dtype=torch.uint8, device="cuda")
-            w.stack.capture()
-            pers_ms, _ = time_graph(torch, w.stack, 10, 3)
-            cmp["persistent_graph_ms"] = round(pers_ms, 4)
+            if model.mlp == "swiglu":   # the persistent step runs SiLU-GLU blocks only
+                w.stack.destroy()
+                w.stack.mode = lr.STACK_PERSISTENT
+                w.stack._desc = None
+                need = lr.Stack.scratch_bytes(args.M, w.layers, lr.STACK_PERSISTENT)
+                w.stack.scratch = torch.zeros(need, dtype=torch.uint8, device="cuda")
+                w.stack.capture()
+                pers_ms, _ = time_graph(torch, w.stack, 10, 3)
+                cmp["persistent_graph_ms"] = round(pers_ms, 4)
             line["graph_vs_eager"] = cmp
         layers = w.layers
         w.free()
@@ -610,7 +626,7 @@ def main():
         torch.cuda.empty_cache()
         if not args.no_extras:
             sweep = {}
-            for M in ((1, 8, 32, 64) if model.name == "llama7b" else (1, 16, 64, 256)):
+            for M in ((1, 8, 32, 64) if model.name != "llama70b" else (1, 16, 64, 256)):
                 ww = Workload(torch, lr, M, args.layers, seed=0, model=model, layers=layers)
                 ww.stack.capture()
                 t, _ = time_graph(torch, ww.stack, max(10, args.steps // 2), 3)
@@ -625,7 +641,8 @@ def main():
             if model.name == "llama7b":
                 pre = time_prefill(torch, lr)
             else:
-                pre = time_prefill(torch, lr, M=8 * 4096, rhos=(0.4,), m=model)
+                pre = time_prefill(torch, lr, M=8 * 4096 if model.name == "llama70b" else 16384,
+                                   rhos=(0.4,), m=model)
             for v in pre.values():
                 v["frac_of_bf16_peak"] = round(v["tflops"] / tf, 4)
             line["prefill"] = pre
