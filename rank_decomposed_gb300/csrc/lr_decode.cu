@@ -49,6 +49,17 @@ constexpr int decode_smem_bytes() {
   return DecodeCfg<NT>::kStages * (kWBytes + NT * kBK * 2) + 1024;
 }
 
+// After the MMAs the ring holds the fp32 partial tile [NT][128] and, behind
+// it, the staged output slice of at most ceil(NT / 2) tokens (S >= 2); with
+// S == 1 it holds the staged [NT][128] tile alone.
+template <int NT>
+constexpr bool decode_epilogue_fits() {
+  return NT * kTileN * 4 + ((NT + 1) / 2) * kTileN * 4 <= DecodeCfg<NT>::kStages * (kWBytes + NT * kBK * 2);
+}
+static_assert(decode_epilogue_fits<16>() && decode_epilogue_fits<32>() && decode_epilogue_fits<64>() &&
+                  decode_epilogue_fits<128>() && decode_epilogue_fits<256>(),
+              "decode epilogue staging does not fit in the ring");
+
 __device__ __forceinline__ int act_col(const DecodeProblem& P, int kb) {
   const int k = kb * kBK;
   if (P.gqa_head_dim > 0) {
@@ -112,12 +123,33 @@ __device__ __forceinline__ void store_out4(const DecodeProblem& P, int m, int n,
   }
 }
 
+// Bytes of one output element.
+__device__ __forceinline__ int out_elem_bytes(const DecodeProblem& P) {
+  return P.epi == EPI_STORE_BF16 ? 2 : 4;
+}
+
+// Token `tok` of the tile, staged in shared memory as 128 consecutive output
+// elements, goes to out[tok][n0 ..] with one bulk copy (a bulk fp32 add at L2
+// for the residual epilogue); rows past N are not written.  Needs vec_ok.
+__device__ __forceinline__ void store_staged_row(const DecodeProblem& P, int tok, int n0,
+                                                 const uint8_t* row) {
+  const int esz = out_elem_bytes(P);
+  const int rows = P.N - n0 < kTileN ? P.N - n0 : kTileN;
+  uint8_t* dst = static_cast<uint8_t*>(P.out) + (static_cast<int64_t>(tok) * P.ldo + n0) * esz;
+  if (P.epi == EPI_ADD_F32)
+    bulk_add_f32(dst, row, static_cast<uint32_t>(rows * esz));
+  else
+    bulk_store(dst, row, static_cast<uint32_t>(rows * esz));
+}
+
 // Sum tokens [t0, t1) x 128 rows of the tile over the S partial tiles of the
 // cluster, in rank order, four rows at a time; CH chunks per iteration keep
-// CH * S remote loads in flight.
+// CH * S remote loads in flight.  With `stage` the sums are written there as
+// [t1 - t0][128] output elements (the residual add is left to the bulk copy);
+// without it they are stored to the output directly.
 template <int CH, int MAXS>
 __device__ __forceinline__ void reduce_slice(const DecodeProblem& P, const float* ptile, int S,
-                                             int t0, int t1, int n0, int et) {
+                                             int t0, int t1, int n0, int et, uint8_t* stage) {
   const int nchunks = (t1 - t0) * (kTileN / 4);
   const uint32_t pbase = smem_u32(ptile);
   uint32_t rbase[MAXS];
@@ -152,7 +184,17 @@ __device__ __forceinline__ void reduce_slice(const DecodeProblem& P, const float
           acc.z += v[h][s2].z;
           acc.w += v[h][s2].w;
         }
-      store_out4(P, tok, n0 + row, acc);
+      if (stage == nullptr) {
+        store_out4(P, tok, n0 + row, acc);
+      } else if (P.epi == EPI_STORE_BF16) {
+        const uint32_t lo = static_cast<uint32_t>(f32_to_bf16_rn(acc.x)) |
+                            (static_cast<uint32_t>(f32_to_bf16_rn(acc.y)) << 16);
+        const uint32_t hi = static_cast<uint32_t>(f32_to_bf16_rn(acc.z)) |
+                            (static_cast<uint32_t>(f32_to_bf16_rn(acc.w)) << 16);
+        *reinterpret_cast<uint2*>(stage + ((tok - t0) * kTileN + row) * 2) = make_uint2(lo, hi);
+      } else {
+        *reinterpret_cast<float4*>(stage + ((tok - t0) * kTileN + row) * 4) = acc;
+      }
     }
   }
 }
@@ -165,6 +207,10 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
   constexpr uint32_t kStageBytes = kWBytes + kABytes;
   constexpr uint32_t kTmemCols = NT < 32 ? 32 : NT;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kTileN, NT);
+  // Outputs of the 128- and 256-token shapes are staged in shared memory and
+  // written by bulk copies; smaller ones are stored by the threads (measured
+  // faster at those sizes).
+  constexpr bool kBulkEpi = NT >= 128;
 
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -181,7 +227,14 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
 #pragma unroll
   for (int i = 1; i < kMaxGroup; ++i)
     if (i < p.n_problems && item >= p.prob[i].item_begin) g = i;
-  const DecodeProblem& P = p.prob[g];
+  // A register copy of this CTA's problem, selected with static indices.  A
+  // reference into the parameter array at a run-time index is a generic
+  // pointer, and the compiler would re-read every field after each global
+  // store of the epilogue (it cannot prove the two disjoint).
+  DecodeProblem P = p.prob[0];
+#pragma unroll
+  for (int i = 1; i < kMaxGroup; ++i)
+    if (i == g) P = p.prob[i];
   const int local = item - P.item_begin;
   const int tile = local / S;
   const int split = local % S;  // == rank inside the cluster
@@ -225,14 +278,21 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_a = l2_policy_evict_last();
       const int npre = nk < kStages ? nk : kStages;
-      // Weight tiles do not depend on earlier kernels: request them first.
-      for (int i = 0; i < npre; ++i) {
+      const int nw = npre < p.prefetch ? npre : p.prefetch;
+      // Weight tiles do not depend on earlier kernels: the first `nw` are
+      // requested before the wait for the previous kernel.
+      for (int i = 0; i < nw; ++i) {
         mbar_arrive_expect_tx(&full_bar[i], kStageBytes);
         tma_load_2d(w_smem + i * kWBytes, mw, &full_bar[i], (kb0 + i) * kBK, n0, pol_w);
       }
       pdl_wait();
-      for (int i = 0; i < npre; ++i)
+      for (int i = 0; i < nw; ++i)
         tma_load_2d(a_smem + i * kABytes, ma, &full_bar[i], act_col(P, kb0 + i), 0, pol_a);
+      for (int i = nw; i < npre; ++i) {
+        mbar_arrive_expect_tx(&full_bar[i], kStageBytes);
+        tma_load_2d(w_smem + i * kWBytes, mw, &full_bar[i], (kb0 + i) * kBK, n0, pol_w);
+        tma_load_2d(a_smem + i * kABytes, ma, &full_bar[i], act_col(P, kb0 + i), 0, pol_a);
+      }
       int issued = npre;
       for (int i = npre; i < nk; ++i) {
         const int s = i % kStages;
@@ -275,12 +335,43 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
     }
   } else if (S == 1) {
     // Epilogue, whole K in this CTA: TMEM lanes 32*(warp%4) .. +31 hold weight
-    // rows, the columns are tokens; store straight to the output.
+    // rows, the columns are tokens.
     const int q = warp & 3;
     const int n = n0 + q * 32 + lane;
     bool ok = mbar_wait(&accum_bar, 0, &abort_sh);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+    // One decision for all four epilogue warps: the staged path below meets
+    // at a named barrier, which every one of them must reach.
+    ok = named_bar_and(1, 128, ok);
+    if (ok && kBulkEpi && P.vec_ok) {
+      // Stage the tile as [token][128 rows] of output elements in the (now
+      // idle) ring, then one bulk copy per token row.
+      tc_fence_after();
+      uint8_t* stage = smem;
+      const int row = q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < NT / 16; ++c) {
+        if (c * 16 >= p.M) break;
+        uint32_t r[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = c * 16 + j;
+          if (P.epi == EPI_STORE_BF16)
+            reinterpret_cast<uint16_t*>(stage)[tok * kTileN + row] = f32_to_bf16_rn(__uint_as_float(r[j]));
+          else
+            reinterpret_cast<uint32_t*>(stage)[tok * kTileN + row] = r[j];
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      pdl_wait();  // outputs (e.g. the residual stream) belong to earlier kernels
+      const int et = threadIdx.x - 64;
+      const int esz = out_elem_bytes(P);
+      for (int t = et; t < p.M; t += 128) store_staged_row(P, t, n0, stage + t * kTileN * esz);
+      bulk_commit();
+      bulk_wait_all();
+    } else if (ok) {
       tc_fence_after();
       pdl_wait();  // outputs (e.g. the residual stream) belong to earlier kernels
 #pragma unroll 1
@@ -355,14 +446,27 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
     const int et = threadIdx.x - 64;
     const int t0 = split * p.M / S;
     const int t1 = (split + 1) * p.M / S;
-    if (S <= 8)
-      reduce_slice<2, 8>(P, ptile, S, t0, t1, n0, et);
+    // The reduced slice is staged behind the partial tile (which the other
+    // CTAs of the cluster are still reading) and leaves by bulk copies.
+    uint8_t* stage = (kBulkEpi && P.vec_ok) ? smem + NT * kTileN * 4 : nullptr;
+    if (S <= 4)
+      reduce_slice<4, 4>(P, ptile, S, t0, t1, n0, et, stage);
+    else if (S <= 8)
+      reduce_slice<2, 8>(P, ptile, S, t0, t1, n0, et, stage);
     else
-      reduce_slice<1, kMaxCluster>(P, ptile, S, t0, t1, n0, et);
+      reduce_slice<1, kMaxCluster>(P, ptile, S, t0, t1, n0, et, stage);
+    if (stage != nullptr) {
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      const int esz = out_elem_bytes(P);
+      for (int t = et; t < t1 - t0; t += 128) store_staged_row(P, t0 + t, n0, stage + t * kTileN * esz);
+      bulk_commit();
+    }
   }
 
   __syncwarp();
   cluster_sync_all();  // no CTA leaves while others read its shared memory
+  if (kBulkEpi && warp >= 2 && P.vec_ok) bulk_wait_all();  // staged rows have been written
   }
   tc_fence_before();
   __syncthreads();
@@ -385,8 +489,17 @@ int env_int(const char* name, int dflt) {
 // LR_DECODE_SPLITS forces a split count (a measurement switch).
 int choose_splits(const GemmOp* ops, int n_ops, int slots, int M) {
   static const int forced = env_int("LR_DECODE_SPLITS", 0);
-  constexpr double overhead = 16.0;
-  constexpr double red = 0.5;
+  double overhead = 16.0;
+  double red = 0.5;
+  // LR_DECODE_COST="overhead,red" replaces the two weights (a measurement
+  // switch, read at every launch).
+  if (const char* c = getenv("LR_DECODE_COST")) {
+    double o2 = 0.0, r2 = 0.0;
+    if (sscanf(c, "%lf,%lf", &o2, &r2) == 2) {
+      overhead = o2;
+      red = r2;
+    }
+  }
   int tiles = 0, min_nkb = 1 << 30;
   for (int g = 0; g < n_ops; ++g) {
     tiles += (ops[g].N + kTileN - 1) / kTileN;
@@ -435,6 +548,10 @@ lr_status launch_nt(int M, const GemmOp* ops, int n_ops, int32_t* status, cudaSt
   prm.status = status;
   const int S = choose_splits(ops, n_ops, DecodeCfg<NT>::kSlots, M);
   prm.splits = S;
+  // Weight stages requested before griddepcontrol.wait (LR_DECODE_PREFETCH
+  // overrides it: a measurement switch, read at every launch).
+  const int pf = env_int("LR_DECODE_PREFETCH", -1);
+  prm.prefetch = pf >= 0 ? std::min(pf, DecodeCfg<NT>::kStages) : DecodeCfg<NT>::kStages;
   // Fault injection for the timeout path (tests only): read at every launch.
   prm.stall_producer = env_int("LR_TEST_STALL_PRODUCER", 0) != 0 ? 1 : 0;
   int items = 0;

@@ -64,6 +64,7 @@ struct DecodeParams {
   int32_t n_problems;
   int32_t splits;       // K splits per tile == cluster size
   int32_t stall_producer;  // fault-injection hook: the TMA producer issues nothing
+  int32_t prefetch;     // weight stages requested before waiting for the previous kernel
   int32_t* status;
   DecodeProblem prob[kMaxGroup];
 };
