@@ -45,6 +45,7 @@ MODELS = {
     "opt30b": Model("opt30b", 7168, 28672, 56, 56, 128, 48, mlp="relu"),
 }
 LLAMA7B = MODELS["llama7b"]
+LLAMA70B = MODELS["llama70b"]
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -434,6 +435,80 @@ def time_kv_reconstruct(torch, lr, m=LLAMA7B, n_seq=64, reps=5):
             "gbs": round(nbytes / best / 1e9, 1)}
 
 
+def rank_sharding(torch, lr, M=64, Gs=(2, 4, 8), rho=RHO, m=None, reps=20):
+    """The low-rank communication scheme of the pages, simulated on this GPU.
+
+    Per layer of the LLaMA-70B-shaped stack (the model the pages analyse), the
+    collective bytes that the busiest of G processes receives: the rank-space
+    all-gather of every down-projection output t, against the all-reduce of
+    every full-width output y that a naive split of the two factors needs.
+    Then the gate projection run as G simulated processes on this GPU (their
+    launches one after another, the all-gather as device copies) against the
+    plain two-launch linear.
+    """
+    m = LLAMA70B if m is None else m
+    names = ["q", "k", "v", "o", "gate", "up", "down"]
+    sh = shapes(rho, m)
+    acct = {}
+    for G in Gs:
+        tot_r = tot_f = 0
+        per = {}
+        for name, s_ in zip(names, sh):
+            if s_ is None:
+                continue
+            _, d_out, r = s_
+            if 64 * G > min(r, d_out):
+                per[name] = None
+                continue
+            rs, fs = lr.rank_shard_comm_bytes(M, d_out, r, G, 2)
+            per[name] = {"rank_space_bytes": rs, "full_space_bytes": fs}
+            tot_r += rs
+            tot_f += fs
+        acct[str(G)] = {"rank_space_bytes": tot_r, "full_space_bytes": tot_f,
+                        "reduction": round(1.0 - tot_r / tot_f, 4), "per_linear": per}
+    d_in, d_out, r = sh[4]
+    sa, sg = synth.factor_stds(d_in, r)
+    At = torch.empty((r, d_in), dtype=torch.bfloat16, device="cuda")
+    Bt = torch.empty((d_out, r), dtype=torch.bfloat16, device="cuda")
+    cs = torch.from_numpy(synth.sigma_scale(r)).cuda()
+    synth.fill_bf16_normal_device(At.data_ptr(), r, d_in, 3, synth.make_tag(0, 4, synth.KIND_A), sa)
+    synth.fill_bf16_normal_device(Bt.data_ptr(), d_out, r, 3, synth.make_tag(0, 4, synth.KIND_B), sg, cs.data_ptr())
+    x = torch.empty((M, d_in), dtype=torch.bfloat16, device="cuda")
+    synth.fill_bf16_normal_device(x.data_ptr(), M, d_in, 3, synth.make_tag(0, 0, synth.KIND_X), 1.0)
+    f = lr.FactorPair(At, Bt)
+    y = torch.empty((M, d_out), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def timeit(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    ws = torch.zeros(lr.linear_workspace_bytes(M, f), dtype=torch.uint8, device="cuda")
+    plain_ms = timeit(lambda: lr.linear_forward(x, f, y, ws, st))
+    sim = {}
+    for G in Gs:
+        wsg = torch.zeros(lr.rank_sharded_workspace_bytes(M, f, G), dtype=torch.uint8, device="cuda")
+        ms = timeit(lambda: lr.linear_forward_rank_sharded(x, f, G, y, wsg, st))
+        sim[str(G)] = {"ms_all_processes": round(ms, 4), "ms_per_process": round(ms / G, 4),
+                       "gather_copy_bytes": M * r * 2}
+    if int(st.item()) != 0:
+        raise SystemExit("rank_sharding status %d" % int(st.item()))
+    return {"model": m.name, "M": M, "rho": rho, "elem_bytes": 2,
+            "collective_bytes_per_layer_busiest_process": acct,
+            "simulated_gate": {"shape": [d_in, d_out, r], "plain_ms": round(plain_ms, 4),
+                               "sharded": sim,
+                               "note": "all G processes run on this one GPU in turn; per-process time is "
+                                       "their average, not a multi-GPU measurement"}}
+
+
 def oracle_sample(M, layers_sample, seed=0, rho=RHO, m=LLAMA7B):
     """Time the fp64 oracle on M rows through `layers_sample` layers (factor generation untimed)."""
     import oracle
@@ -647,6 +722,7 @@ def main():
                 v["frac_of_bf16_peak"] = round(v["tflops"] / tf, 4)
             line["prefill"] = pre
             line["kv_reconstruct"] = time_kv_reconstruct(torch, lr, m=model)
+            line["rank_sharding"] = rank_sharding(torch, lr)
         if not args.no_cpu:
             sample_layers = min(8, args.layers)
             tcpu, n = oracle_sample(args.M, sample_layers, m=model)

@@ -224,6 +224,46 @@ lr_status lr_kv_reconstruct(const void* latent_pool, int64_t pool_rows, int32_t 
                             int32_t* dev_status, lr_stream s);
 
 /* ---------------------------------------------------------------------------
+ * Rank-space sharding of one factorized linear, simulated on this GPU (English
+ * page section 2.A, "Highly Efficient Low-Rank Communication": the down
+ * projection is split by columns and its output all-gathered in the low-rank
+ * space; the up projection runs in shard mode, with no reduce-sum).
+ *
+ * The rank columns are split over G simulated processes in blocks of 64: process g
+ * owns rank columns R_g = [64*floor(g*nr/G), 64*floor((g+1)*nr/G)) with
+ * nr = r/64, and output columns O_g likewise over d_out/64 blocks.  Then
+ *   1. down, per process:  t_g = x A_r[:, R_g]   into process g's own buffer
+ *      (bf16 [M][|R_g|], the rows R_g of At);
+ *   2. all-gather in rank space, emulated by device-to-device copies of every
+ *      t_g into the columns R_g of one gathered t (bf16 [M][r]);
+ *   3. up, shard mode, per process:  y[:, O_g] = t B_r[:, O_g]  (the rows O_g
+ *      of Bt), written straight into the caller's y.
+ * Every launch is issued on `s`, one process after another.  y equals
+ * lr_linear_forward's result up to the fp32 summation order of the split GEMMs.
+ * Arguments and checks as lr_linear_forward, plus 1 <= n_shards <= r/64 and
+ * n_shards <= d_out/64 (else LR_ERR_INVALID_ARG); the workspace (device,
+ * 256-byte aligned, caller-owned) holds the G process buffers and the
+ * gathered t: lr_rank_sharded_workspace_bytes bytes.  M == 0 is a no-op. */
+size_t lr_rank_sharded_workspace_bytes(int64_t M, const lr_factor* f, int32_t n_shards);
+lr_status lr_linear_forward_rank_sharded(const void* x, int64_t ldx, void* y, int64_t ldy,
+                                         lr_dtype y_dtype, int64_t M, const lr_factor* f,
+                                         int32_t n_shards, void* workspace, size_t ws_bytes,
+                                         int32_t* dev_status, lr_stream s);
+
+/* lr_rank_shard_comm_bytes (host only): collective bytes that the busiest of
+ * the G processes receives for one factorized linear, with the column split
+ * above and elements of elem_bytes bytes:
+ *   *rank_space = (r - min_g |R_g|) * M * elem_bytes    (ring all-gather of t,
+ *                 the low-rank scheme);
+ *   *full_space = 2 (d_out - min_g |O_g|) * M * elem_bytes  (ring all-reduce of
+ *                 y, i.e. reduce-scatter then all-gather: the reduce-sum in the
+ *                 full dimension that a naive split of the two factors needs).
+ * LR_ERR_INVALID_ARG on a negative M, non-positive sizes, r or d_out not a
+ * multiple of 64, or n_shards outside [1, min(r, d_out)/64]. */
+lr_status lr_rank_shard_comm_bytes(int64_t M, int32_t d_out, int32_t r, int32_t n_shards,
+                                   int32_t elem_bytes, int64_t* rank_space, int64_t* full_space);
+
+/* ---------------------------------------------------------------------------
  * A decode step of a layer stack over fixed buffers (English page section 2.C:
  * addresses and launch parameters stay fixed while the logical batch changes):
  *   xbuf = remap_compact(pool_in); h = widen(xbuf); for each layer:

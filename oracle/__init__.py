@@ -237,3 +237,65 @@ def kv_reconstruct(latent_pool: np.ndarray, remap, n_active: int, cap: int, B: n
     """
     buf, bad = remap_gather(latent_pool, remap, n_active, cap)
     return buf, np.asarray(buf, dtype=np.float64) @ np.asarray(B, dtype=np.float64), bad
+
+
+# ------------------------------------------------------ rank-space sharding
+def shard_columns(n: int, G: int):
+    """Split n columns (a multiple of 64) over G processes in whole 64-column blocks.
+
+    Process g gets [64 * floor(g * nb / G), 64 * floor((g + 1) * nb / G)) with
+    nb = n / 64: contiguous, as even as whole blocks allow, in process order.
+    """
+    nb = n // 64
+    return [(64 * (nb * g // G), 64 * (nb * (g + 1) // G)) for g in range(G)]
+
+
+def rank_sharded_linear(x, A, B, G: int):
+    """The low-rank communication scheme for one factorized linear (English page, section 2.A).
+
+    The down projection is split by columns over G processes, its outputs are
+    all-gathered in the rank dimension so every process holds the same t, and
+    the up projection runs in shard mode: process g computes only its own
+    block of output columns, so no reduce-sum is needed.  Returns
+    (per-process t_g, gathered t, y).  fp64, no rounding.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    t_parts = [x @ A[:, a:b] for a, b in shard_columns(A.shape[1], G)]
+    t = np.concatenate(t_parts, axis=1)
+    y = np.concatenate([t @ B[:, a:b] for a, b in shard_columns(B.shape[1], G)], axis=1)
+    return t_parts, t, y
+
+
+def ring_allgather_received(chunk_cols, M: int, elem_bytes: int):
+    """Bytes each process receives in a ring all-gather of an [M][sum(chunk_cols)] matrix.
+
+    Process g starts with chunk g.  In step s = 0 .. G-2 every process passes
+    the chunk it received in the previous step (its own in step 0) to its
+    right neighbour, so process g receives chunk (g - s - 1) mod G.
+    """
+    G = len(chunk_cols)
+    recv = [0] * G
+    for s in range(G - 1):
+        for g in range(G):
+            recv[g] += chunk_cols[(g - s - 1) % G] * M * elem_bytes
+    return recv
+
+
+def ring_allreduce_received(chunk_cols, M: int, elem_bytes: int):
+    """Bytes each process receives in a ring all-reduce (reduce-scatter, then all-gather).
+
+    Reduce-scatter: in step s process g receives the running partial sum of
+    chunk (g - s - 1) mod G from its left neighbour and adds its own part, so
+    after G-1 steps each chunk is fully reduced on one process.  The
+    all-gather phase then circulates the reduced chunks as in
+    ring_allgather_received.  Both phases move whole chunks.
+    """
+    G = len(chunk_cols)
+    recv = [0] * G
+    for s in range(G - 1):  # reduce-scatter
+        for g in range(G):
+            recv[g] += chunk_cols[(g - s - 1) % G] * M * elem_bytes
+    gather = ring_allgather_received(chunk_cols, M, elem_bytes)
+    return [a + b for a, b in zip(recv, gather)]

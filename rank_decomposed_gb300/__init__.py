@@ -84,6 +84,10 @@ def _load():
         "remap_scatter": (i32, [vp, vp, vp, vp, i64, i64, i64, vp, vp]),
         "remap_build": (i32, [vp, i64, vp, i32, i32, i32, i64, vp, vp, vp]),
         "lr_kv_reconstruct": (i32, [vp, i64, i32, vp, vp, i64, vp, vp, i32, vp, vp, vp]),
+        "lr_rank_sharded_workspace_bytes": (sz, [i64, P(Factor), i32]),
+        "lr_linear_forward_rank_sharded": (i32, [vp, i64, vp, i64, i32, i64, P(Factor), i32, vp, sz,
+                                                 vp, vp]),
+        "lr_rank_shard_comm_bytes": (i32, [i64, i32, i32, i32, i32, P(i64), P(i64)]),
         "lr_stack_forward": (i32, [P(StackDesc), vp]),
         "lr_graph_capture": (i32, [P(StackDesc), P(vp)]),
         "lr_graph_replay": (i32, [vp, vp]),
@@ -205,6 +209,41 @@ def linear_forward(x, f: FactorPair, y, workspace, status, stream=None):
                                workspace.numel() * workspace.element_size(), _ptr(status),
                                _stream(stream))
     _check("lr_linear_forward", st)
+
+
+def rank_sharded_workspace_bytes(M: int, f: FactorPair, n_shards: int) -> int:
+    fc = f.c()
+    return int(lib.lr_rank_sharded_workspace_bytes(M, ctypes.byref(fc), n_shards))
+
+
+def linear_forward_rank_sharded(x, f: FactorPair, n_shards: int, y, workspace, status, stream=None):
+    """y = (x A_r) B_r computed as n_shards simulated processes of the rank-space scheme.
+
+    Each process runs the down projection on its block of rank columns, the
+    blocks are all-gathered (device copies) into one t, and each process runs
+    the up projection on its block of output columns.
+    """
+    import torch
+    _bf16(x, "x")
+    if y.dim() != 2 or y.stride(1) != 1:
+        raise ValueError("y must be a row-major 2-D tensor")
+    ydt = {torch.bfloat16: LR_BF16, torch.float32: LR_F32}.get(y.dtype)
+    if ydt is None:
+        raise TypeError("y must be bfloat16 or float32")
+    fc = f.c()
+    st = lib.lr_linear_forward_rank_sharded(x.data_ptr(), x.stride(0), y.data_ptr(), y.stride(0), ydt,
+                                            x.shape[0], ctypes.byref(fc), n_shards, workspace.data_ptr(),
+                                            workspace.numel() * workspace.element_size(), _ptr(status),
+                                            _stream(stream))
+    _check("lr_linear_forward_rank_sharded", st)
+
+
+def rank_shard_comm_bytes(M: int, d_out: int, r: int, n_shards: int, elem_bytes: int = 2):
+    """(rank-space all-gather bytes, full-space all-reduce bytes) received by the busiest process."""
+    a, b = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check("lr_rank_shard_comm_bytes",
+           lib.lr_rank_shard_comm_bytes(M, d_out, r, n_shards, elem_bytes, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
 
 
 NOALLOC_SCRATCH_BYTES = 4 << 20

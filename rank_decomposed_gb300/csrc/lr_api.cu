@@ -779,6 +779,106 @@ lr_status lr_kv_reconstruct(const void* latent_pool, int64_t pool_rows, int32_t 
   return run_ops(cap, &up, 1, dev_status, cs);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Columns [shard_begin(g), shard_begin(g + 1)) of an n-column dimension (n a
+// multiple of 64) belong to process g of G: whole 64-column blocks, as even as
+// possible.
+int64_t shard_begin(int64_t n, int g, int G) { return 64 * ((n / 64) * g / G); }
+
+}  // namespace
+
+extern "C" {
+
+size_t lr_rank_sharded_workspace_bytes(int64_t M, const lr_factor* f, int32_t n_shards) {
+  if (f == nullptr || M < 0 || n_shards < 1 || f->r < 64 * n_shards) return 0;
+  const size_t m = static_cast<size_t>(M);
+  size_t total = align_up(m * static_cast<size_t>(f->r) * 2);
+  for (int g = 0; g < n_shards; ++g) {
+    const int64_t w = shard_begin(f->r, g + 1, n_shards) - shard_begin(f->r, g, n_shards);
+    total += align_up(m * static_cast<size_t>(w) * 2);
+  }
+  return total;
+}
+
+lr_status lr_linear_forward_rank_sharded(const void* x, int64_t ldx, void* y, int64_t ldy,
+                                         lr_dtype y_dtype, int64_t M, const lr_factor* f,
+                                         int32_t n_shards, void* workspace, size_t ws_bytes,
+                                         int32_t* dev_status, lr_stream s) {
+  lr_status st = check_factor(f, "rank_sharded");
+  if (st != LR_OK) return st;
+  const int G = n_shards;
+  if (G < 1 || 64 * G > f->r || 64 * G > f->d_out)
+    return invalid("rank_sharded: n_shards=%d outside [1, min(r, d_out)/64]", G);
+  if (M < 0 || M > (int64_t(1) << 31) - 1) return invalid("rank_sharded: bad M");
+  if (M == 0) return LR_OK;
+  if (x == nullptr || y == nullptr || workspace == nullptr) return invalid("rank_sharded: null pointer");
+  if (y_dtype != LR_BF16 && y_dtype != LR_F32) return invalid("rank_sharded: bad y dtype");
+  if (ldx < f->d_in || ldx % 8 || !aligned16(x))
+    return invalid("rank_sharded: x must be 16-byte aligned with ldx >= d_in, ldx %% 8 == 0");
+  if (ldy < f->d_out) return invalid("rank_sharded: ldy < d_out");
+  if (M > kDecodeMaxRows && (!aligned16(y) || ldy % 8))
+    return invalid("rank_sharded: y must be 16-byte aligned with ldy %% 8 == 0");
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return invalid("rank_sharded: workspace not 256-byte aligned");
+  if (ws_bytes < lr_rank_sharded_workspace_bytes(M, f, G)) return invalid("rank_sharded: workspace too small");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+  const size_t m = static_cast<size_t>(M);
+  uint8_t* t = static_cast<uint8_t*>(workspace);  // gathered [M][r]
+  uint8_t* local = t + align_up(m * static_cast<size_t>(f->r) * 2);
+  const int esz = y_dtype == LR_BF16 ? 2 : 4;
+  const uint16_t* At = static_cast<const uint16_t*>(f->At);
+  const uint16_t* Bt = static_cast<const uint16_t*>(f->Bt);
+  // 1. down projection of every process into its own buffer
+  uint8_t* tg = local;
+  for (int g = 0; g < G; ++g) {
+    const int64_t r0 = shard_begin(f->r, g, G), w = shard_begin(f->r, g + 1, G) - r0;
+    GemmOp down = make_op(At + r0 * f->d_in, static_cast<int>(w), f->d_in, x, ldx, f->d_in,
+                          EPI_STORE_BF16, tg, w);
+    st = run_ops(M, &down, 1, dev_status, cs);
+    if (st != LR_OK) return st;
+    tg += align_up(m * static_cast<size_t>(w) * 2);
+  }
+  // 2. all-gather in rank space: every t_g lands in its columns of t
+  tg = local;
+  for (int g = 0; g < G; ++g) {
+    const int64_t r0 = shard_begin(f->r, g, G), w = shard_begin(f->r, g + 1, G) - r0;
+    cudaError_t e = cudaMemcpy2DAsync(t + r0 * 2, static_cast<size_t>(f->r) * 2, tg,
+                                      static_cast<size_t>(w) * 2, static_cast<size_t>(w) * 2, m,
+                                      cudaMemcpyDeviceToDevice, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "rank_sharded: all-gather copy");
+    tg += align_up(m * static_cast<size_t>(w) * 2);
+  }
+  // 3. up projection of every process on its output columns (shard mode)
+  for (int g = 0; g < G; ++g) {
+    const int64_t o0 = shard_begin(f->d_out, g, G), w = shard_begin(f->d_out, g + 1, G) - o0;
+    GemmOp up = make_op(Bt + o0 * f->r, static_cast<int>(w), f->r, t, f->r, f->r,
+                        y_dtype == LR_BF16 ? EPI_STORE_BF16 : EPI_STORE_F32,
+                        static_cast<uint8_t*>(y) + o0 * esz, ldy);
+    st = run_ops(M, &up, 1, dev_status, cs);
+    if (st != LR_OK) return st;
+  }
+  return LR_OK;
+}
+
+lr_status lr_rank_shard_comm_bytes(int64_t M, int32_t d_out, int32_t r, int32_t n_shards,
+                                   int32_t elem_bytes, int64_t* rank_space, int64_t* full_space) {
+  if (rank_space == nullptr || full_space == nullptr) return invalid("comm_bytes: null output");
+  if (M < 0 || d_out <= 0 || r <= 0 || elem_bytes <= 0) return invalid("comm_bytes: bad sizes");
+  if (r % 64 || d_out % 64) return invalid("comm_bytes: r and d_out must be multiples of 64");
+  const int G = n_shards;
+  if (G < 1 || 64 * G > r || 64 * G > d_out) return invalid("comm_bytes: bad n_shards");
+  int64_t min_r = r, min_o = d_out;
+  for (int g = 0; g < G; ++g) {
+    min_r = std::min(min_r, shard_begin(r, g + 1, G) - shard_begin(r, g, G));
+    min_o = std::min(min_o, shard_begin(d_out, g + 1, G) - shard_begin(d_out, g, G));
+  }
+  *rank_space = (r - min_r) * M * elem_bytes;
+  *full_space = 2 * (d_out - min_o) * M * elem_bytes;
+  return LR_OK;
+}
+
 lr_status remap_build(const int32_t* lengths, int64_t n_seq, const int32_t* block_table,
                       int32_t blocks_per_seq, int32_t block_rows, int32_t tail_rows, int64_t cap,
                       int32_t* remap_out, int32_t* n_active_out, int32_t* n_runs_out) {

@@ -154,3 +154,47 @@ def test_graph_handles_checked():
     assert lr.lib.lr_graph_destroy(None) == lr.LR_ERR_STATE
     g = ctypes.c_void_p()
     assert lr.lib.lr_graph_capture(None, ctypes.byref(g)) == lr.LR_ERR_INVALID_ARG
+
+
+# ------------------------------------------------- rank-space sharding (host)
+@pytest.mark.parametrize("d_out,r", [(8192, 2432), (1024, 576), (28672, 3840), (8192, 3840),
+                                     (4096, 1216), (11008, 1792), (512, 64)])
+def test_rank_shard_comm_bytes_matches_ring_simulation(d_out, r):
+    """The closed forms equal the busiest process of a step-by-step ring simulation."""
+    M, e = 64, 2
+    for G in range(1, 10):
+        if 64 * G > min(r, d_out):
+            with pytest.raises(lr.LrError):
+                lr.rank_shard_comm_bytes(M, d_out, r, G, e)
+            continue
+        rs, fs = lr.rank_shard_comm_bytes(M, d_out, r, G, e)
+        rchunks = [b - a for a, b in oracle.shard_columns(r, G)]
+        ochunks = [b - a for a, b in oracle.shard_columns(d_out, G)]
+        assert rs == max(oracle.ring_allgather_received(rchunks, M, e))
+        assert fs == max(oracle.ring_allreduce_received(ochunks, M, e))
+
+
+def test_rank_shard_comm_bytes_errors():
+    out = (ctypes.c_int64(), ctypes.c_int64())
+    call = lambda *a: lr.lib.lr_rank_shard_comm_bytes(*a, ctypes.byref(out[0]), ctypes.byref(out[1]))
+    assert call(4, 512, 128, 2, 2) == lr.LR_OK
+    assert call(-1, 512, 128, 2, 2) == lr.LR_ERR_INVALID_ARG
+    assert call(4, 500, 128, 2, 2) == lr.LR_ERR_INVALID_ARG
+    assert call(4, 512, 128, 3, 2) == lr.LR_ERR_INVALID_ARG   # 3 shards of 2 rank blocks
+    assert call(4, 512, 128, 0, 2) == lr.LR_ERR_INVALID_ARG
+    assert lr.lib.lr_rank_shard_comm_bytes(4, 512, 128, 2, 2, None, None) == lr.LR_ERR_INVALID_ARG
+
+
+def test_rank_sharded_argument_checks_launch_nothing():
+    f = _fake_factor(512, 1024, 256)
+    ws = lr.lib.lr_rank_sharded_workspace_bytes(5, ctypes.byref(f), 3)
+    # gathered t [5][256] plus shards of 64, 64 and 128 rank columns, each 256-byte aligned
+    assert ws == 2560 + 768 + 768 + 1280
+    assert lr.lib.lr_rank_sharded_workspace_bytes(5, ctypes.byref(f), 5) == 0  # 5 > 256/64
+    call = lambda M, G, ws_bytes=1 << 30, y=0x2000: lr.lib.lr_linear_forward_rank_sharded(
+        0x1000, 512, y, 1024, lr.LR_F32, M, ctypes.byref(f), G, 0x300000, ws_bytes, None, None)
+    assert call(0, 2) == lr.LR_OK                        # M = 0: no-op
+    assert call(4, 0) == lr.LR_ERR_INVALID_ARG
+    assert call(4, 5) == lr.LR_ERR_INVALID_ARG           # more shards than rank blocks
+    assert call(4, 2, ws_bytes=100) == lr.LR_ERR_INVALID_ARG
+    assert call(4, 2, y=0) == lr.LR_ERR_INVALID_ARG

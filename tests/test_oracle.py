@@ -293,3 +293,70 @@ def test_block_relu_mlp_path():
     want = out["h1"] + np.where(n2 > 0, n2, 0.0)
     assert np.allclose(out["h2"], want, rtol=0, atol=1e-15)
     assert np.array_equal(oracle.relu(np.array([-2.0, -0.0, 0.0, 3.5])), [0.0, 0.0, 0.0, 3.5])
+
+
+# ------------------------------------------------- rank-space sharding
+@pytest.mark.parametrize("n,G", [(64, 1), (256, 2), (2432, 8), (576, 9), (3840, 7), (1216, 19)])
+def test_shard_columns_partition(n, G):
+    """Contiguous, in process order, whole 64-column blocks, sizes within one block of each other."""
+    parts = oracle.shard_columns(n, G)
+    assert len(parts) == G
+    assert parts[0][0] == 0 and parts[-1][1] == n
+    for (a, b), (c, _) in zip(parts, parts[1:]):
+        assert b == c
+    sizes = [b - a for a, b in parts]
+    assert all(s % 64 == 0 and s >= 64 for s in sizes)
+    assert max(sizes) - min(sizes) <= 64
+
+
+def test_rank_sharded_exact_integers():
+    """Small-integer inputs make every fp64 product and sum exact: the sharded
+    scheme must reproduce the exact integer product x A B, its t_g must be the
+    exact columns of x A, and every G gives the same answer."""
+    rng = np.random.default_rng(5)
+    x = rng.integers(-3, 4, size=(3, 128)).astype(np.float64)
+    A = rng.integers(-2, 3, size=(128, 320)).astype(np.float64)
+    B = rng.integers(-2, 3, size=(320, 192)).astype(np.float64)
+    xi = [[int(v) for v in row] for row in x]
+    Ai = [[int(v) for v in row] for row in A]
+    Bi = [[int(v) for v in row] for row in B]
+    t_exact = [[sum(xi[m][k] * Ai[k][j] for k in range(128)) for j in range(320)] for m in range(3)]
+    y_exact = [[sum(t_exact[m][j] * Bi[j][o] for j in range(320)) for o in range(192)] for m in range(3)]
+    for G in (1, 2, 3, 5):
+        t_parts, t, y = oracle.rank_sharded_linear(x, A, B, G)
+        assert np.array_equal(t, np.array(t_exact, dtype=np.float64))
+        assert np.array_equal(y, np.array(y_exact, dtype=np.float64))
+        for (a, b), tg in zip(oracle.shard_columns(320, G), t_parts):
+            assert np.array_equal(tg, np.array(t_exact, dtype=np.float64)[:, a:b])
+
+
+def test_rank_sharded_equals_unsharded_bf16():
+    """On bf16-valued inputs the sharded result equals the plain (x A) B to fp64 rounding."""
+    x = _bf16_matrix(3, 40, (5, 256))
+    A = _bf16_matrix(3, 41, (256, 384), 1 / 16)
+    B = _bf16_matrix(3, 42, (384, 512), 1 / 20)
+    _, y_ref = oracle.lowrank_linear(x, A, B)
+    for G in (1, 2, 4, 6):
+        _, _, y = oracle.rank_sharded_linear(x, A, B, G)
+        assert np.allclose(y, y_ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_ring_collectives_equal_chunks(G):
+    """Equal chunks: an all-gather delivers the (G-1) chunks a process lacks,
+    (G-1)/G of the matrix; a ring all-reduce moves twice that; one process moves nothing."""
+    n, M, e = 64 * 8 * 3, 7, 2
+    chunks = [n // G] * G
+    ag = oracle.ring_allgather_received(chunks, M, e)
+    ar = oracle.ring_allreduce_received(chunks, M, e)
+    assert ag == [(G - 1) * n // G * M * e] * G
+    assert ar == [2 * (G - 1) * n // G * M * e] * G
+
+
+def test_ring_allgather_delivers_every_other_chunk_once():
+    """Uneven chunks: process g receives exactly the chunks it does not own, once each."""
+    chunks = [64, 128, 192, 64, 320]
+    M, e = 3, 2
+    ag = oracle.ring_allgather_received(chunks, M, e)
+    for g in range(len(chunks)):
+        assert ag[g] == (sum(chunks) - chunks[g]) * M * e
