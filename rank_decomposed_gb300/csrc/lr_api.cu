@@ -291,13 +291,12 @@ lr_status enqueue_block(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws
     LR_TRY(run_ops(M, up, 2, status, s));
     LR_TRY(launch_silu_mul(ws + L.g, ws + L.u, ws + L.a, M, dff, s));
   } else {
-    // non-GLU: a = relu(LR_up(n2))
+    // non-GLU: a = relu(LR_up(n2)), the ReLU applied in the GEMM's epilogue
     const lr_factor& fu = f[LR_UP];
     GemmOp ud = make_op(fu.At, fu.r, d, n2, d, d, EPI_STORE_BF16, t[LR_UP], fu.r);
-    GemmOp uu = make_op(fu.Bt, dff, fu.r, t[LR_UP], fu.r, fu.r, EPI_STORE_BF16, ws + L.u, dff);
+    GemmOp uu = make_op(fu.Bt, dff, fu.r, t[LR_UP], fu.r, fu.r, EPI_RELU_BF16, ws + L.a, dff);
     LR_TRY(run_ops(M, &ud, 1, status, s));
     LR_TRY(run_ops(M, &uu, 1, status, s));
-    LR_TRY(launch_relu(ws + L.u, ws + L.a, M, dff, s));
   }
   {
     const lr_factor& fd = f[LR_DOWN];
@@ -311,9 +310,11 @@ lr_status enqueue_block(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws
 }
 
 int64_t block_launches(int64_t M, const lr_block_desc* b) {
-  // rmsnorm x2, silu_mul or relu, and the GEMM launches (grouped for decode sizes).
-  if (M <= kDecodeMaxRows) return 3 + 8;
-  return 3 + (b->mlp == LR_MLP_RELU ? 12 : 14);
+  // rmsnorm x2, the GEMM launches (grouped at decode sizes) and, for SiLU-GLU,
+  // a silu_mul launch; ReLU is applied in the up projection's epilogue.
+  const int64_t glu = b->mlp == LR_MLP_RELU ? 0 : 1;
+  if (M <= kDecodeMaxRows) return 2 + glu + 8;
+  return 2 + glu + (b->mlp == LR_MLP_RELU ? 12 : 14);
 }
 
 // ---------------------------------------------------------------- stack

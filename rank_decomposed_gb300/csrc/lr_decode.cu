@@ -92,10 +92,15 @@ __device__ __forceinline__ void cluster_sync_all() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ float relu_f(float v) { return v > 0.0f ? v : 0.0f; }
+
 // Four consecutive outputs (m, n .. n+3) of one problem.
 __device__ __forceinline__ void store_out4(const DecodeProblem& P, int m, int n, float4 v) {
   const int64_t off = static_cast<int64_t>(m) * P.ldo + n;
-  if (P.epi == EPI_STORE_BF16) {
+  if (P.epi == EPI_RELU_BF16) {
+    v.x = relu_f(v.x); v.y = relu_f(v.y); v.z = relu_f(v.z); v.w = relu_f(v.w);
+  }
+  if (epi_is_bf16(P.epi)) {
     uint16_t* o = static_cast<uint16_t*>(P.out) + off;
     const uint16_t b0 = f32_to_bf16_rn(v.x), b1 = f32_to_bf16_rn(v.y);
     const uint16_t b2 = f32_to_bf16_rn(v.z), b3 = f32_to_bf16_rn(v.w);
@@ -125,7 +130,7 @@ __device__ __forceinline__ void store_out4(const DecodeProblem& P, int m, int n,
 
 // Bytes of one output element.
 __device__ __forceinline__ int out_elem_bytes(const DecodeProblem& P) {
-  return P.epi == EPI_STORE_BF16 ? 2 : 4;
+  return epi_is_bf16(P.epi) ? 2 : 4;
 }
 
 // Token `tok` of the tile, staged in shared memory as 128 consecutive output
@@ -186,7 +191,10 @@ __device__ __forceinline__ void reduce_slice(const DecodeProblem& P, const float
         }
       if (stage == nullptr) {
         store_out4(P, tok, n0 + row, acc);
-      } else if (P.epi == EPI_STORE_BF16) {
+      } else if (epi_is_bf16(P.epi)) {
+        if (P.epi == EPI_RELU_BF16) {
+          acc.x = relu_f(acc.x); acc.y = relu_f(acc.y); acc.z = relu_f(acc.z); acc.w = relu_f(acc.w);
+        }
         const uint32_t lo = static_cast<uint32_t>(f32_to_bf16_rn(acc.x)) |
                             (static_cast<uint32_t>(f32_to_bf16_rn(acc.y)) << 16);
         const uint32_t hi = static_cast<uint32_t>(f32_to_bf16_rn(acc.z)) |
@@ -357,9 +365,11 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int tok = c * 16 + j;
-          if (P.epi == EPI_STORE_BF16)
-            reinterpret_cast<uint16_t*>(stage)[tok * kTileN + row] = f32_to_bf16_rn(__uint_as_float(r[j]));
-          else
+          if (epi_is_bf16(P.epi)) {
+            const float v = __uint_as_float(r[j]);
+            reinterpret_cast<uint16_t*>(stage)[tok * kTileN + row] =
+                f32_to_bf16_rn(P.epi == EPI_RELU_BF16 ? relu_f(v) : v);
+          } else
             reinterpret_cast<uint32_t*>(stage)[tok * kTileN + row] = r[j];
         }
       }
@@ -398,9 +408,13 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
               if (j < nt) o[static_cast<int64_t>(c * 16 + j) * P.ldo] = __uint_as_float(r[j]);
           } else {
             uint16_t* o = static_cast<uint16_t*>(P.out) + n;
+            const bool rl = P.epi == EPI_RELU_BF16;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (j < nt) o[static_cast<int64_t>(c * 16 + j) * P.ldo] = f32_to_bf16_rn(__uint_as_float(r[j]));
+              if (j < nt) {
+                const float v = __uint_as_float(r[j]);
+                o[static_cast<int64_t>(c * 16 + j) * P.ldo] = f32_to_bf16_rn(rl ? relu_f(v) : v);
+              }
           }
         }
       }

@@ -166,25 +166,6 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__
 }
 
 // a = bf16(max(u, 0)), 8 elements per vector.
-__global__ void __launch_bounds__(256) relu_kernel(const uint4* __restrict__ u, uint4* __restrict__ a,
-                                                   int64_t n8) {
-  pdl_launch_dependents();
-  pdl_wait();
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const uint4 v = u[i];
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      // a negative bf16 has its sign bit set: clear such halves (keeps +0, drops -0)
-      const uint32_t lo = (w[j] & 0x8000u) ? 0u : (w[j] & 0xFFFFu);
-      const uint32_t hi = (w[j] & 0x80000000u) ? 0u : (w[j] & 0xFFFF0000u);
-      w[j] = lo | hi;
-    }
-    a[i] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
 __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ in,
                                                     float4* __restrict__ out, int64_t n8) {
   pdl_launch_dependents();
@@ -336,13 +317,6 @@ lr_status launch_silu_mul(const void* g, const void* u, void* out, int64_t M, in
   return launch(silu_mul_kernel, dim3(elementwise_grid(n8)), dim3(256), s, "silu_mul",
                 static_cast<const uint4*>(g), static_cast<const uint4*>(u),
                 static_cast<uint4*>(out), n8);
-}
-
-lr_status launch_relu(const void* u, void* out, int64_t M, int d, cudaStream_t s) {
-  const int64_t n8 = M * d / 8;
-  if (n8 == 0) return LR_OK;
-  return launch(relu_kernel, dim3(elementwise_grid(n8)), dim3(256), s, "relu",
-                static_cast<const uint4*>(u), static_cast<uint4*>(out), n8);
 }
 
 lr_status launch_widen(const void* in_bf16, float* out, int64_t n, cudaStream_t s) {

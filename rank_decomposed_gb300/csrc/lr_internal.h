@@ -26,7 +26,12 @@ enum Epilogue : int32_t {
   EPI_STORE_BF16 = 0,  // out_bf16[m*ldo + n] = rne(v)
   EPI_STORE_F32 = 1,   // out_f32[m*ldo + n] = v
   EPI_ADD_F32 = 2,     // out_f32[m*ldo + n] += v   (residual stream)
+  EPI_RELU_BF16 = 3,   // out_bf16[m*ldo + n] = rne(max(v, 0))   (non-GLU MLP)
 };
+
+__host__ __device__ inline bool epi_is_bf16(int32_t epi) {
+  return epi == EPI_STORE_BF16 || epi == EPI_RELU_BF16;
+}
 
 // One problem of a GEMM launch:  out[m][n] = sum_k act[m][k] * W[n][k]
 // for m < M, n < N, k < K (K a multiple of 64).  W and act are bf16.
@@ -157,12 +162,12 @@ int num_sms();
 // Launchers (lr_decode.cu, lr_prefill.cu, lr_glue.cu).  They assume their
 // arguments were validated by the caller.
 lr_status launch_decode(int M, const GemmOp* ops, int n_ops, int32_t* status, cudaStream_t s);
+
 lr_status launch_prefill(int64_t M, const GemmOp& op, int32_t* status, cudaStream_t s);
 lr_status launch_rmsnorm(const float* h, void* out_bf16, int64_t M, int d, float eps,
                          cudaStream_t s);
 lr_status launch_silu_mul(const void* g, const void* u, void* out, int64_t M, int d,
                           cudaStream_t s);
-lr_status launch_relu(const void* u, void* out, int64_t M, int d, cudaStream_t s);
 lr_status launch_widen(const void* in_bf16, float* out, int64_t n, cudaStream_t s);
 lr_status launch_narrow(const float* in, void* out_bf16, int64_t n, cudaStream_t s);
 // Stack glue, one CTA per row: gather + widen, and narrow + scatter.

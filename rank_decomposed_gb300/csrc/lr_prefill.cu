@@ -187,7 +187,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         if (m < p.M) {
           const int64_t off = static_cast<int64_t>(m) * p.ldo + n;
-          if (p.epi == EPI_STORE_BF16) {
+          if (epi_is_bf16(p.epi)) {
+            if (p.epi == EPI_RELU_BF16) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (__uint_as_float(r[j]) < 0.0f) r[j] = 0u;
+            }
             uint32_t w[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
