@@ -215,9 +215,9 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
   constexpr uint32_t kStageBytes = kWBytes + kABytes;
   constexpr uint32_t kTmemCols = NT < 32 ? 32 : NT;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kTileN, NT);
-  // Outputs of the 128- and 256-token shapes are staged in shared memory and
-  // written by bulk copies; smaller ones are stored by the threads (measured
-  // faster at those sizes).
+  // Unsplit tiles, and split tiles of the 128- and 256-token shapes, are
+  // staged in shared memory and written by bulk copies; split tiles of the
+  // smaller shapes are stored by the threads (measured faster there).
   constexpr bool kBulkEpi = NT >= 128;
 
   __shared__ __align__(8) uint64_t full_bar[kStages];
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
     // One decision for all four epilogue warps: the staged path below meets
     // at a named barrier, which every one of them must reach.
     ok = named_bar_and(1, 128, ok);
-    if (ok && kBulkEpi && P.vec_ok) {
+    if (ok && P.vec_ok) {
       // Stage the tile as [token][128 rows] of output elements in the (now
       // idle) ring, then one bulk copy per token row.
       tc_fence_after();
