@@ -219,6 +219,8 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
   // staged in shared memory and written by bulk copies; split tiles of the
   // smaller shapes are stored by the threads (measured faster there).
   constexpr bool kBulkEpi = NT >= 128;
+  // TMEM column chunks (16 tokens each) loaded before one wait in the epilogue.
+  constexpr int kChunksPerWait = NT / 16 < 4 ? NT / 16 : 4;
 
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -357,21 +359,26 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
       uint8_t* stage = smem;
       const int row = q * 32 + lane;
 #pragma unroll 1
-      for (int c = 0; c < NT / 16; ++c) {
-        if (c * 16 >= p.M) break;
-        uint32_t r[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, r);
+      for (int c0 = 0; c0 < NT / 16; c0 += kChunksPerWait) {
+        if (c0 * 16 >= p.M) break;
+        uint32_t r[kChunksPerWait][16];
+#pragma unroll
+        for (int b = 0; b < kChunksPerWait; ++b)
+          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + (c0 + b) * 16, r[b]);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int tok = c * 16 + j;
-          if (epi_is_bf16(P.epi)) {
-            const float v = __uint_as_float(r[j]);
-            reinterpret_cast<uint16_t*>(stage)[tok * kTileN + row] =
-                f32_to_bf16_rn(P.epi == EPI_RELU_BF16 ? relu_f(v) : v);
-          } else
-            reinterpret_cast<uint32_t*>(stage)[tok * kTileN + row] = r[j];
-        }
+        for (int b = 0; b < kChunksPerWait; ++b)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = (c0 + b) * 16 + j;
+            if (epi_is_bf16(P.epi)) {
+              const float v = __uint_as_float(r[b][j]);
+              reinterpret_cast<uint16_t*>(stage)[tok * kTileN + row] =
+                  f32_to_bf16_rn(P.epi == EPI_RELU_BF16 ? relu_f(v) : v);
+            } else {
+              reinterpret_cast<uint32_t*>(stage)[tok * kTileN + row] = r[b][j];
+            }
+          }
       }
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
@@ -432,16 +439,20 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
     if (ok) {
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < NT / 16; ++c) {
-        if (c * 16 >= p.M) break;
-        uint32_t r[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, r);
+      for (int c0 = 0; c0 < NT / 16; c0 += kChunksPerWait) {
+        if (c0 * 16 >= p.M) break;
+        uint32_t r[kChunksPerWait][16];
+#pragma unroll
+        for (int b = 0; b < kChunksPerWait; ++b)
+          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + (c0 + b) * 16, r[b]);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int tok = c * 16 + j;
-          if (tok < p.M) ptile[tok * kTileN + row] = __uint_as_float(r[j]);
-        }
+        for (int b = 0; b < kChunksPerWait; ++b)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = (c0 + b) * 16 + j;
+            if (tok < p.M) ptile[tok * kTileN + row] = __uint_as_float(r[b][j]);
+          }
       }
     } else if (lane == 0) {
       abort_sh = 1;
