@@ -31,7 +31,9 @@
 namespace lr {
 namespace {
 
-constexpr int kThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
+// warp 0: TMA, warp 1: MMA, warps 2..5: epilogue (TMEM lane quadrants 2, 3,
+// 0, 1); all six warps share the split-K reduction.
+constexpr int kThreads = 192;
 constexpr int kTileN = 128;    // weight rows per tile = MMA M
 constexpr int kBK = 64;        // reduction depth of one pipeline stage
 constexpr int kWBytes = kTileN * kBK * 2;
@@ -148,24 +150,25 @@ __device__ __forceinline__ void store_staged_row(const DecodeProblem& P, int tok
 }
 
 // Sum tokens [t0, t1) x 128 rows of the tile over the S partial tiles of the
-// cluster, in rank order, four rows at a time; CH chunks per iteration keep
-// CH * S remote loads in flight.  With `stage` the sums are written there as
+// cluster, in rank order, four rows at a time, by `nthr` threads (et is this
+// thread's index among them); CH chunks per iteration keep CH * S remote loads
+// in flight.  With `stage` the sums are written there as
 // [t1 - t0][128] output elements (the residual add is left to the bulk copy);
 // without it they are stored to the output directly.
 template <int CH, int MAXS>
 __device__ __forceinline__ void reduce_slice(const DecodeProblem& P, const float* ptile, int S,
-                                             int t0, int t1, int n0, int et, uint8_t* stage) {
+                                             int t0, int t1, int n0, int et, int nthr, uint8_t* stage) {
   const int nchunks = (t1 - t0) * (kTileN / 4);
   const uint32_t pbase = smem_u32(ptile);
   uint32_t rbase[MAXS];
 #pragma unroll
   for (int s2 = 0; s2 < MAXS; ++s2)
     rbase[s2] = s2 < S ? cluster_addr(pbase, static_cast<uint32_t>(s2)) : 0u;
-  for (int c = et; c < nchunks; c += 128 * CH) {
+  for (int c = et; c < nchunks; c += nthr * CH) {
     float4 v[CH][MAXS];
 #pragma unroll
     for (int h = 0; h < CH; ++h) {
-      const int cc = c + h * 128;
+      const int cc = c + h * nthr;
       if (cc < nchunks) {
         const uint32_t off = static_cast<uint32_t>(((t0 + cc / 32) * kTileN + (cc % 32) * 4) * 4);
 #pragma unroll
@@ -175,7 +178,7 @@ __device__ __forceinline__ void reduce_slice(const DecodeProblem& P, const float
     }
 #pragma unroll
     for (int h = 0; h < CH; ++h) {
-      const int cc = c + h * 128;
+      const int cc = c + h * nthr;
       if (cc >= nchunks) break;
       const int tok = t0 + cc / 32;
       const int row = (cc % 32) * 4;
@@ -464,34 +467,35 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
   __syncwarp();
   cluster_sync_all();  // every partial tile of the cluster is in shared memory
 
-  if (warp >= 2) {
+  {
     // Reduce this CTA's share of the tile -- tokens [t0, t1) x 128 rows -- over
-    // the S partial tiles of the cluster.
+    // the S partial tiles of the cluster, with every warp of the CTA (the
+    // producer and MMA warps are done by now).
     pdl_wait();  // outputs (e.g. the residual stream) belong to earlier kernels
-    const int et = threadIdx.x - 64;
+    const int et = threadIdx.x;
     const int t0 = split * p.M / S;
     const int t1 = (split + 1) * p.M / S;
     // The reduced slice is staged behind the partial tile (which the other
     // CTAs of the cluster are still reading) and leaves by bulk copies.
     uint8_t* stage = (kBulkEpi && P.vec_ok) ? smem + NT * kTileN * 4 : nullptr;
     if (S <= 4)
-      reduce_slice<4, 4>(P, ptile, S, t0, t1, n0, et, stage);
+      reduce_slice<4, 4>(P, ptile, S, t0, t1, n0, et, kThreads, stage);
     else if (S <= 8)
-      reduce_slice<2, 8>(P, ptile, S, t0, t1, n0, et, stage);
+      reduce_slice<2, 8>(P, ptile, S, t0, t1, n0, et, kThreads, stage);
     else
-      reduce_slice<1, kMaxCluster>(P, ptile, S, t0, t1, n0, et, stage);
+      reduce_slice<1, kMaxCluster>(P, ptile, S, t0, t1, n0, et, kThreads, stage);
     if (stage != nullptr) {
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kThreads);
       const int esz = out_elem_bytes(P);
-      for (int t = et; t < t1 - t0; t += 128) store_staged_row(P, t0 + t, n0, stage + t * kTileN * esz);
+      for (int t = et; t < t1 - t0; t += kThreads) store_staged_row(P, t0 + t, n0, stage + t * kTileN * esz);
       bulk_commit();
     }
   }
 
   __syncwarp();
   cluster_sync_all();  // no CTA leaves while others read its shared memory
-  if (kBulkEpi && warp >= 2 && P.vec_ok) bulk_wait_all();  // staged rows have been written
+  if (kBulkEpi && P.vec_ok) bulk_wait_all();  // staged rows have been written
   }
   tc_fence_before();
   __syncthreads();
