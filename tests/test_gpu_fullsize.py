@@ -1,0 +1,56 @@
+"""Parity at the benchmark's own size and launch configuration.
+
+The LLaMA-7B-shaped 32-layer decomposed stack at rho = 0.4, 64 rows compacted
+by remap from the paged pool, replayed as one CUDA graph -- the decode step
+bench.py times -- against the fp64 oracle on sampled rows.  Rows do not
+interact (one-token attention), so the oracle follows each sampled row alone
+through all 32 layers, regenerating every layer's factors on the host from the
+same seeded recipe.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from lr_testutil import assert_parity, host_bits
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+import rank_decomposed_gb300 as lr  # noqa: E402
+
+
+def test_llama7b_32_layer_graph_step_sampled_rows():
+    import bench
+    m, M = bench.LLAMA7B, 64
+    w = bench.Workload(torch, lr, M, m.layers)
+    try:
+        w.stack.capture()
+        w.stack.replay()
+        torch.cuda.synchronize()
+        assert int(w.stack.status.item()) == 0
+        h = w.stack.h.cpu().numpy().astype(np.float64)
+        y_bits = host_bits(w.stack.ybuf)
+        remap = w.stack.remap.cpu().numpy()
+        n = w.n_active
+        assert n == M
+        # the step's output rows land in the pool at their remap rows, as bf16 of h
+        out_rows = host_bits(w.stack.pool_out[w.stack.remap[:n].long()])
+        assert np.array_equal(out_rows, y_bits[:n])
+        pool_rows = w.stack.pool_in.shape[0]
+    finally:
+        w.free()
+        torch.cuda.empty_cache()
+
+    rows = [0, 17, 63]
+    pool = synth.bf16_normal(0, synth.make_tag(0, 0, synth.KIND_POOL), (pool_rows, m.d), 1.0)
+    x = oracle.widen_bf16(pool[remap[rows]])
+    del pool
+    hr = x
+    for layer in range(m.layers):
+        factors = {}
+        for p, (a, b, r) in enumerate(bench.shapes(bench.RHO, m)):
+            At, Bt = synth.factor_pair(0, layer, p, a, b, r)
+            factors[synth.PROJ_NAMES[p]] = oracle.factor_from_stored(At, Bt)
+        hr = oracle.block_forward(hr, factors, m.nh, m.nkv, m.hd)
+    assert_parity(h[rows], hr, "7B 32-layer graph step, rows %s" % rows)
