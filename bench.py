@@ -105,7 +105,8 @@ def load_peaks():
         with open(path) as f:
             p = json.load(f)
         hbm = p.get("hbm_gbs")
-        tf = p.get("bf16_tflops_sustained") or p.get("bf16_tflops")
+        # the prefill leg times a few milliseconds of GEMMs at a time: the burst figure
+        tf = p.get("bf16_tflops") or p.get("bf16_tflops_sustained")
         if hbm and tf:
             return float(hbm), float(tf), "measured"
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
