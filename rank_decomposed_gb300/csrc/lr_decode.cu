@@ -10,9 +10,11 @@
 //    multi-stage mbarrier ring; one thread issues the MMAs;
 //  * the K dimension of each 128-row tile is split over the CTAs of one
 //    thread-block cluster; their fp32 partial tiles are summed in a fixed
-//    order through distributed shared memory, so no workspace, no counters
-//    and no floating-point atomics are involved and the result is
-//    deterministic;
+//    order through distributed shared memory, by all six warps once the main
+//    loop is done, so no workspace, no counters and no floating-point atomics
+//    are involved and the result is deterministic;
+//  * an unsplit tile leaves TMEM through a shared-memory staging tile and one
+//    bulk copy per token row (a bulk fp32 add for the residual stream);
 //  * up to three problems with the same input (q/k/v, gate/up) share one
 //    launch;
 //  * programmatic dependent launch: weight tiles (which never depend on the
