@@ -155,6 +155,16 @@ def test_stack_eager_graph_and_remap(mode):
         ref = _oracle_stack(cfg, hosts, pool_bits, perm, n2)
         assert_parity(stack.h[:n2].cpu().numpy(), ref, "stack replay n=%d" % n2)
         assert not torch.any(stack.h[n2:])
+
+    # an empty batch: every row of the fixed buffer is padding and nothing is scattered
+    stack.n_active.fill_(0)
+    stack.pool_out.copy_(stack.pool_in)
+    stack.h.fill_(5.0)
+    stack.replay()
+    torch.cuda.synchronize()
+    assert int(stack.status.item()) == 0
+    assert not torch.any(stack.h)
+    assert torch.equal(stack.pool_out, stack.pool_in)
     stack.destroy()
 
 

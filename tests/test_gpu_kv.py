@@ -72,4 +72,10 @@ def test_kv_reconstruct_graph_replays_new_batches():
         _, out_ref, _ = oracle.kv_reconstruct(oracle.widen_bf16(pool_bits), rm, k, cap, B)
         assert_parity(bf16_f64(out)[:k], out_ref[:k], "kv replay %d" % trial)
         assert not torch.any(out[k:].float())
+    # an empty batch: the fixed-size GEMM runs over padding only
+    d_remap.fill_(-1)
+    d_n.fill_(0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert not torch.any(out.float()) and not torch.any(buf.float())
     assert int(st.item()) == 0
