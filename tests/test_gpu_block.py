@@ -260,3 +260,24 @@ def test_stack_with_per_layer_ranks():
     ref = _oracle_stack(SMALL, list(hosts), pool_bits, remap, n)
     assert_parity(stack.h[:n].cpu().numpy(), ref, "variadic-rank stack")
     stack.destroy()
+
+
+@pytest.mark.parametrize("cfg_name,cap", [("glu", 16), ("relu", 16), ("glu", 300), ("relu", 300)])
+def test_launch_count_matches_the_kernels_launched(cfg_name, cap):
+    """lr_stack_launch_count (the bench's gpu_launches) against the kernels the profiler sees."""
+    profiler = torch.profiler
+    cfg = SMALL if cfg_name == "glu" else OPT_SMALL
+    stack, *_ = _make_stack(cfg, 2, cap, min(cap, 12), seed=15, mode=lr.STACK_LAYERED)
+    stack.forward()                    # first use: configuration outside the profiled step
+    torch.cuda.synchronize()
+    for _ in range(2):                 # the first session of a process may record nothing
+        with profiler.profile(activities=[profiler.ProfilerActivity.CUDA]) as prof:
+            stack.forward()
+            torch.cuda.synchronize()
+    assert int(stack.status.item()) == 0
+    kernels = [e for e in prof.events()
+               if e.device_type == torch.autograd.DeviceType.CUDA
+               and "memcpy" not in e.name.lower() and "memset" not in e.name.lower()]
+    if not kernels:
+        pytest.skip("the profiler recorded no device activity here")
+    assert len(kernels) == stack.launch_count(), sorted({e.name[:40] for e in kernels})
