@@ -50,6 +50,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_w) {
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
+  // The last N tile of a width that is not a multiple of kBN (N is a multiple
+  // of 64) runs a narrower MMA instead of multiplying zero-filled rows.
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ __align__(8) uint64_t accf_bar[2];
@@ -133,6 +135,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem + b * kBN;
+        int m0t, n0t;
+        tile_coords(p, t, m0t, n0t);
+        const uint32_t idesc = p.N - n0t >= kBN ? kIdesc : idesc_bf16_f32(kBM, p.N - n0t);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&full_bar[s], (it / kStages) & 1, &abort_sh)) {
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd = smem_desc_sw128(sa + kABytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            tc_mma_bf16(d, ad + 2 * k, bd + 2 * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            tc_mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
           tc_commit(&empty_bar[s]);
         }
         tc_commit(&accf_bar[b]);
