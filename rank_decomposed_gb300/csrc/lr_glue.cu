@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint4* __restrict__
   }
 }
 
-// a = bf16(max(u, 0)), 8 elements per vector.
+// out = fp32(in), 8 bf16 elements per vector.
 __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ in,
                                                     float4* __restrict__ out, int64_t n8) {
   pdl_launch_dependents();
