@@ -515,13 +515,14 @@ int env_int(const char* name, int dflt) {
 // Pick the number of K splits (= cluster size) of a launch: minimise, in units
 // of one 128 x 64 weight tile, the per-SM share of weight tiles, plus a fixed
 // cost per wave of CTAs (launch, pipeline fill, epilogue) and the cluster
-// reduction, which reads S partial tiles of M tokens.  The two weights were
-// fitted by sweeping them on the 7B-shaped decode step (M = 1..64).
+// reduction, which reads S partial tiles of M tokens.  The weights were fitted
+// by sweeping them on the 7B- and 70B-shaped decode steps: the reduction
+// weighs more for the 256-token shape, which runs one CTA per SM.
 // LR_DECODE_SPLITS forces a split count (a measurement switch).
 int choose_splits(const GemmOp* ops, int n_ops, int slots, int M) {
   static const int forced = env_int("LR_DECODE_SPLITS", 0);
   double overhead = 16.0;
-  double red = 0.5;
+  double red = slots == 1 ? 1.25 : 0.5;
   // LR_DECODE_COST="overhead,red" replaces the two weights (a measurement
   // switch, read at every launch).
   if (const char* c = getenv("LR_DECODE_COST")) {
