@@ -667,7 +667,7 @@ def main():
         "config": {"workload": workload, "model": "%s-shaped factorized stack (random factors)" % model.name,
                    "global_batch": int(tokens), "seq_len": 1, "rows_per_gpu": args.M,
                    "layers": args.layers, "rho": RHO, "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs larger than L2: %.2f GB of factors streamed per step" % (step_bytes(args.M, args.layers, m=model) / 1e9),
+                   "l2": "inputs larger than L2: %.2f GB of factors and activations streamed per step" % (step_bytes(args.M, args.layers, m=model) / 1e9),
                    "remap_runs": w.n_runs},
         "clocks": ck, "gpu_launches": launches, "graph_ms_by_n_active": n_active_check,
         "step_hbm_gbs": round(step_bytes(args.M, args.layers, m=model) / (ms * 1e-3) / 1e9, 1),
