@@ -129,17 +129,28 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % index)
+        # the raw samples go to a temporary file; LR_CLOCKS_CSV keeps them at a chosen path
+        self.keep = os.environ.get("LR_CLOCKS_CSV")
+        self.path = None
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            import tempfile
+            if self.keep:
+                self.path = self.keep
+            else:
+                fd, self.path = tempfile.mkstemp(prefix="clocks_%d_" % self.index, suffix=".csv")
+                os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            if getattr(self, "f", None) is not None:
+                self.f.close()
+            if self.path and not self.keep and os.path.exists(self.path):
+                os.remove(self.path)
 
     def stop(self):
         if self.proc is None:
@@ -161,6 +172,8 @@ class Clocks:
             for n, v in zip(names, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+        if not self.keep:
+            os.remove(self.path)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
