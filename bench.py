@@ -126,8 +126,11 @@ class Clocks:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, uuid=None):
+        # nvidia-smi ignores CUDA_VISIBLE_DEVICES: select the GPU by its UUID
+        # when torch reports one, so the samples come from the GPU in use
         self.index = index
+        self.select = uuid if uuid else str(index)
         self.proc = None
         # the raw samples go to a temporary file; LR_CLOCKS_CSV keeps them at a chosen path
         self.keep = os.environ.get("LR_CLOCKS_CSV")
@@ -142,7 +145,7 @@ class Clocks:
                 fd, self.path = tempfile.mkstemp(prefix="clocks_%d_" % self.index, suffix=".csv")
                 os.close(fd)
             self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.select, "--query-gpu=" + self.QUERY,
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
@@ -177,7 +180,7 @@ class Clocks:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "gpu": self.select}
 
 
 # -------------------------------------------------------------- our arm
@@ -560,6 +563,17 @@ def oracle_sample(M, layers_sample, seed=0, rho=RHO, m=LLAMA7B):
     return total, n
 
 
+def gpu_uuid(torch):
+    """'GPU-<uuid>' of the current device as nvidia-smi names it, or None."""
+    try:
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        return None
+    if not u:
+        return None
+    return u if u.startswith("GPU-") else "GPU-" + u
+
+
 def cpu_threads():
     try:
         import threadpoolctl
@@ -652,7 +666,7 @@ def main():
                           "isolated_gbs": r["bytes"] / r["isolated_s"] / 1e9}))
         return
     w.stack.capture()
-    clocks = Clocks(torch.cuda.current_device() if world == 1 else local)
+    clocks = Clocks(torch.cuda.current_device() if world == 1 else local, gpu_uuid(torch))
     ms, ck = time_graph(torch, w.stack, args.steps, args.warmup, clocks, barrier)
     ms, tokens = aggregate(dist, ms, args.M)
     if int(w.stack.status.item()) != 0:
@@ -750,40 +764,60 @@ def main():
             line["kv_reconstruct"] = time_kv_reconstruct(torch, lr, m=model)
             line["rank_sharding"] = rank_sharding(torch, lr)
         if not args.no_cpu:
-            sample_layers = min(8, args.layers)
+            sample_layers = oracle_sample_layers(args.layers)
             tcpu, n = oracle_sample(args.M, sample_layers, m=model)
             v = n / (tcpu * args.layers / sample_layers)
             line["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": cpu_threads(),
                                     "kind": "oracle",
-                                    "sample": "fp64 oracle over the same %d rows through %d of %d layers "
-                                              "(%.1f s), scaled linearly to the full stack" % (n, sample_layers, args.layers, tcpu)}
+                                    "sample": "fp64 oracle over the same %d rows through %d of %d layers (%.1f s)%s"
+                                              % (n, sample_layers, args.layers, tcpu,
+                                                 "" if sample_layers == args.layers
+                                                 else ", scaled linearly to the full stack")}
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
 
 
+def oracle_sample_layers(n_layers):
+    """Layers of the stack the oracle runs per timed sample (the same in both arms).
+
+    The whole stack when it has at most 32 layers (the 7B and OPT shapes'
+    step, about a second on 16 cores); otherwise 8 layers, whose time is
+    scaled to the full stack (rows are independent and every layer has the
+    same shapes, so the time is linear in the layer count).
+    """
+    return n_layers if n_layers <= 32 else 8
+
+
 def run_reference(args, workload):
-    """The oracle as it stands, on the host cores: each step is 1 layer of the stack for M rows."""
+    """The oracle as it stands, on the host cores: each step is the oracle on M rows
+    through oracle_sample_layers(L) layers of the stack."""
     import oracle  # noqa: F401
     model = MODELS[args.config]
+    ls = oracle_sample_layers(args.layers)
     for _ in range(args.warmup):
-        oracle_sample(args.M, 1, m=model)
+        oracle_sample(args.M, ls, m=model)
     tot, n = 0.0, 0
     for _ in range(args.steps):
-        t, n = oracle_sample(args.M, 1, m=model)
+        t, n = oracle_sample(args.M, ls, m=model)
         tot += t
-    per_layer = tot / args.steps
-    value = n / (per_layer * args.layers)
+    per_step = tot / args.steps                       # measured: what each step ran
+    full = per_step * args.layers / ls                # the whole stack (= per_step when ls == layers)
+    value = n / full
+    sample = ("each step: the fp64 oracle on %d rows through %d of %d layers" % (n, ls, args.layers)
+              + ("" if ls == args.layers else ", time scaled linearly to the full stack"))
     line = {"impl": "reference", "metric": "factorized-linear tokens/s (decode)", "value": round(value, 3),
             "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(per_layer * args.layers * 1e3, 3), "higher_is_better": True,
+            "ms_per_step": round(per_step * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload, "rows": n, "layers": args.layers, "rho": RHO},
+            "config": {"workload": workload, "rows": n, "layers": args.layers, "layers_per_step": ls,
+                       "rho": RHO},
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-                             "sample": "each step: the fp64 oracle on %d rows through 1 of %d layers, "
-                                       "scaled linearly to the full stack" % (n, args.layers)},
+                             "sample": sample},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    if ls != args.layers:
+        line["ms_full_stack_extrapolated"] = round(full * 1e3, 3)
     print(json.dumps(line), flush=True)
 
 

@@ -111,8 +111,9 @@ typedef struct {
  *   kept in `workspace`; the sums accumulate in fp32.  A bf16 y is the
  *   round-to-nearest-even image of the fp32 y.
  *   workspace: device, at least lr_linear_workspace_bytes(M, f) bytes, 256-byte
- *   aligned, zero-filled before its first use; the kernels leave it reusable.
- *   Calls that share a workspace must be ordered on one stream.
+ *   aligned; its contents on entry do not matter (every element that is read
+ *   was written by the same call).  Calls that share a workspace must be
+ *   ordered on one stream.
  *   M = 0 is a no-op.  M <= 256 runs the decode kernels, larger M the prefill
  *   kernels.  The result is deterministic (no floating-point atomics). */
 size_t lr_linear_workspace_bytes(int64_t M, const lr_factor* f);
@@ -158,8 +159,8 @@ lr_status lr_linear_forward_noalloc(const void* x, int64_t ldx, void* y, int64_t
  * Spanish page section 1 (attention and MLP projections decomposed) and
  * section 2 "Generalizacion"; English page section 2.D (MHA/GQA/MQA, GLU MLP).
  * Linear inputs are rounded to bf16.  scratch: device, at least
- * lr_block_scratch_bytes(M, b) bytes, 256-byte aligned, zero-filled before its
- * first use.  M = 0 is a no-op. */
+ * lr_block_scratch_bytes(M, b) bytes, 256-byte aligned; its contents on entry
+ * do not matter.  M = 0 is a no-op. */
 size_t lr_block_scratch_bytes(int64_t M, const lr_block_desc* b);
 lr_status lr_block_forward(float* h, int64_t M, const lr_block_desc* b, void* scratch,
                            size_t scratch_bytes, int32_t* dev_status, lr_stream s);
@@ -321,6 +322,17 @@ int64_t lr_stack_launch_count(const lr_stack_desc* st);
 
 const char* lr_status_string(lr_status st);
 const char* lr_last_error(void);
+
+/* ---------------------------------------------------------------------------
+ * Testing hook (no counterpart on the pages).  lr_test_stall_producer(1) makes
+ * the weight producer of every decode-size GEMM launched afterwards issue no
+ * copy, so the bounded wait of the thread that consumes the copies runs out:
+ * the launch reports LR_ERR_TIMEOUT through dev_status (after about two
+ * seconds), releases its resources and returns, and the context stays usable.
+ * lr_test_stall_producer(0) restores normal launches.  It exists for the
+ * failure-detection tests only; nothing else sets it, and no environment
+ * variable does. */
+void lr_test_stall_producer(int32_t on);
 
 #ifdef __cplusplus
 }

@@ -96,6 +96,7 @@ def _load():
         "lr_stack_scratch_bytes": (sz, [P(StackDesc)]),
         "lr_status_string": (ctypes.c_char_p, [i32]),
         "lr_last_error": (ctypes.c_char_p, []),
+        "lr_test_stall_producer": (None, [i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

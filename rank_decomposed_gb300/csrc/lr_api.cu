@@ -8,6 +8,7 @@
 #include <stdlib.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -47,6 +48,10 @@ int num_sms() {
   }
   return cached[dev];
 }
+
+static std::atomic<int> g_stall_producer{0};
+
+bool test_stall_producer() { return g_stall_producer.load(std::memory_order_relaxed) != 0; }
 
 bool pdl_enabled() {
   static const bool on = [] {
@@ -133,6 +138,8 @@ lr_status invalid(const char* fmt, ...) {
   return LR_ERR_INVALID_ARG;
 }
 
+}  // namespace
+
 lr_status check_factor(const lr_factor* f, const char* name) {
   if (f == nullptr) return invalid("%s: null factor", name);
   if (f->d_in <= 0 || f->d_out <= 0 || f->r <= 0) return invalid("%s: non-positive dims", name);
@@ -174,6 +181,30 @@ lr_status run_ops(int64_t M, const GemmOp* ops, int n, int32_t* status, cudaStre
   }
   return LR_OK;
 }
+
+lr_status check_linear_io(const char* who, const void* x, int64_t ldx, const void* y, int64_t ldy,
+                          lr_dtype y_dtype, int64_t M, const lr_factor* f) {
+  if (x == nullptr || y == nullptr) return invalid("%s: null pointer", who);
+  if (y_dtype != LR_BF16 && y_dtype != LR_F32) return invalid("%s: bad y dtype", who);
+  if (ldx < f->d_in || ldx % 8 || !aligned16(x))
+    return invalid("%s: x must be 16-byte aligned with ldx >= d_in, ldx %% 8 == 0", who);
+  if (ldy < f->d_out) return invalid("%s: ldy < d_out", who);
+  if (M > kDecodeMaxRows && (!aligned16(y) || ldy % 8))
+    return invalid("%s: y must be 16-byte aligned with ldy %% 8 == 0", who);
+  return LR_OK;
+}
+
+lr_status enqueue_linear(const void* x, int64_t ldx, void* y, int64_t ldy, lr_dtype y_dtype,
+                         int64_t M, const lr_factor* f, void* t, int32_t* status, cudaStream_t s) {
+  GemmOp down = make_op(f->At, f->r, f->d_in, x, ldx, f->d_in, EPI_STORE_BF16, t, f->r);
+  GemmOp up = make_op(f->Bt, f->d_out, f->r, t, f->r, f->r,
+                      y_dtype == LR_BF16 ? EPI_STORE_BF16 : EPI_STORE_F32, y, ldy);
+  lr_status st = run_ops(M, &down, 1, status, s);
+  if (st != LR_OK) return st;
+  return run_ops(M, &up, 1, status, s);
+}
+
+namespace {
 
 // ---------------------------------------------------------------- block
 struct BlockLayout {
@@ -684,6 +715,8 @@ const char* lr_status_string(lr_status st) {
 
 const char* lr_last_error(void) { return g_err; }
 
+void lr_test_stall_producer(int32_t on) { g_stall_producer.store(on != 0 ? 1 : 0); }
+
 size_t lr_linear_workspace_bytes(int64_t M, const lr_factor* f) {
   if (f == nullptr || M < 0) return 0;
   return align_up(static_cast<size_t>(M) * static_cast<size_t>(f->r) * 2);
@@ -696,20 +729,13 @@ lr_status lr_linear_forward(const void* x, int64_t ldx, void* y, int64_t ldy, lr
   if (st != LR_OK) return st;
   if (M < 0 || M > (int64_t(1) << 31) - 1) return invalid("linear: bad M");
   if (M == 0) return LR_OK;
-  if (x == nullptr || y == nullptr || workspace == nullptr) return invalid("linear: null pointer");
-  if (y_dtype != LR_BF16 && y_dtype != LR_F32) return invalid("linear: bad y dtype");
-  if (ldx < f->d_in || ldx % 8 || !aligned16(x)) return invalid("linear: x must be 16-byte aligned with ldx >= d_in, ldx %% 8 == 0");
-  if (ldy < f->d_out) return invalid("linear: ldy < d_out");
-  if (M > kDecodeMaxRows && (!aligned16(y) || ldy % 8)) return invalid("linear: y must be 16-byte aligned with ldy %% 8 == 0");
+  st = check_linear_io("linear", x, ldx, y, ldy, y_dtype, M, f);
+  if (st != LR_OK) return st;
+  if (workspace == nullptr) return invalid("linear: null workspace");
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return invalid("linear: workspace not 256-byte aligned");
   if (ws_bytes < lr_linear_workspace_bytes(M, f)) return invalid("linear: workspace too small");
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
-  GemmOp down = make_op(f->At, f->r, f->d_in, x, ldx, f->d_in, EPI_STORE_BF16, workspace, f->r);
-  GemmOp up = make_op(f->Bt, f->d_out, f->r, workspace, f->r, f->r,
-                      y_dtype == LR_BF16 ? EPI_STORE_BF16 : EPI_STORE_F32, y, ldy);
-  st = run_ops(M, &down, 1, dev_status, cs);
-  if (st != LR_OK) return st;
-  return run_ops(M, &up, 1, dev_status, cs);
+  return enqueue_linear(x, ldx, y, ldy, y_dtype, M, f, workspace, dev_status,
+                        reinterpret_cast<cudaStream_t>(s));
 }
 
 size_t lr_block_scratch_bytes(int64_t M, const lr_block_desc* b) {

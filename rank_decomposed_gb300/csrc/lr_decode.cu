@@ -519,18 +519,30 @@ int env_int(const char* name, int dflt) {
 // by sweeping them on the 7B- and 70B-shaped decode steps: the reduction
 // weighs more for the 256-token shape, which runs one CTA per SM.
 // LR_DECODE_SPLITS forces a split count (a measurement switch).
+struct CostOverride {
+  bool set = false;
+  double overhead = 0.0, red = 0.0;
+};
+
+// LR_DECODE_COST="overhead,red" replaces the two weights of the split cost
+// model (a measurement switch, read once per process).
+const CostOverride& cost_override() {
+  static const CostOverride c = [] {
+    CostOverride o;
+    if (const char* v = getenv("LR_DECODE_COST"))
+      o.set = sscanf(v, "%lf,%lf", &o.overhead, &o.red) == 2;
+    return o;
+  }();
+  return c;
+}
+
 int choose_splits(const GemmOp* ops, int n_ops, int slots, int M) {
   static const int forced = env_int("LR_DECODE_SPLITS", 0);
   double overhead = 16.0;
   double red = slots == 1 ? 1.25 : 0.5;
-  // LR_DECODE_COST="overhead,red" replaces the two weights (a measurement
-  // switch, read at every launch).
-  if (const char* c = getenv("LR_DECODE_COST")) {
-    double o2 = 0.0, r2 = 0.0;
-    if (sscanf(c, "%lf,%lf", &o2, &r2) == 2) {
-      overhead = o2;
-      red = r2;
-    }
+  if (cost_override().set) {
+    overhead = cost_override().overhead;
+    red = cost_override().red;
   }
   int tiles = 0, min_nkb = 1 << 30;
   for (int g = 0; g < n_ops; ++g) {
@@ -581,11 +593,11 @@ lr_status launch_nt(int M, const GemmOp* ops, int n_ops, int32_t* status, cudaSt
   const int S = choose_splits(ops, n_ops, DecodeCfg<NT>::kSlots, M);
   prm.splits = S;
   // Weight stages requested before griddepcontrol.wait (LR_DECODE_PREFETCH
-  // overrides it: a measurement switch, read at every launch).
-  const int pf = env_int("LR_DECODE_PREFETCH", -1);
+  // overrides it: a measurement switch, read once per process).
+  static const int pf = env_int("LR_DECODE_PREFETCH", -1);
   prm.prefetch = pf >= 0 ? std::min(pf, DecodeCfg<NT>::kStages) : DecodeCfg<NT>::kStages;
-  // Fault injection for the timeout path (tests only): read at every launch.
-  prm.stall_producer = env_int("LR_TEST_STALL_PRODUCER", 0) != 0 ? 1 : 0;
+  // Fault injection for the timeout path, set only through lr_test_stall_producer.
+  prm.stall_producer = test_stall_producer() ? 1 : 0;
   int items = 0;
   for (int g = 0; g < n_ops; ++g) {
     const GemmOp& o = ops[g];

@@ -151,6 +151,23 @@ struct PersistParams {
 void set_error(const char* fmt, ...);
 lr_status cuda_fail(cudaError_t e, const char* what);
 
+// Argument checks of a factor pair: LR_ERR_INVALID_ARG for null or misaligned
+// pointers and non-positive sizes, LR_ERR_UNSUPPORTED for sizes that are not
+// multiples of 64.  `name` prefixes the message.
+lr_status check_factor(const lr_factor* f, const char* name);
+// Checks of a linear's x / y arguments (pointers, dtype, leading dimensions,
+// alignment) for M > 0 rows.
+lr_status check_linear_io(const char* who, const void* x, int64_t ldx, const void* y, int64_t ldy,
+                          lr_dtype y_dtype, int64_t M, const lr_factor* f);
+GemmOp make_op(const void* W, int N, int K, const void* act, int64_t ld_act, int64_t act_cols,
+               int epi, void* out, int64_t ldo);
+// Ops sharing M: one grouped launch at decode sizes, one launch per op above.
+lr_status run_ops(int64_t M, const GemmOp* ops, int n, int32_t* status, cudaStream_t s);
+// y = (x A_r) B_r with t (bf16 [M][r]) at `t`: the down then the up launch.
+// Arguments already checked.
+lr_status enqueue_linear(const void* x, int64_t ldx, void* y, int64_t ldy, lr_dtype y_dtype,
+                         int64_t M, const lr_factor* f, void* t, int32_t* status, cudaStream_t s);
+
 // Tensor map over a bf16 row-major [rows][cols] matrix with row stride ld
 // (elements), box = box_rows x 64 columns, 128-byte swizzle, zero fill
 // outside the matrix.
@@ -199,5 +216,9 @@ lr_status ensure_configured();
 // Launch attribute helper: programmatic dependent launch on/off for kernels
 // enqueued by this library (on by default).
 bool pdl_enabled();
+
+// Fault-injection hook of the bounded-wait tests (lr_test_stall_producer):
+// while set, the decode kernels' weight producers issue no copy.
+bool test_stall_producer();
 
 }  // namespace lr

@@ -1,13 +1,11 @@
 """Failure detection without a GPU fault: bounded device waits report a status.
 
-The fault is injected on the host side of the launch: with the hook set, the
-decode kernel's TMA producer issues no copy, so the MMA thread's wait on the
-first stage runs out (about two seconds).  The kernel must then report
+The fault is injected on the host side of the launch: with the test hook
+lr_test_stall_producer set, the decode kernel's TMA producer issues no copy,
+so the MMA thread's wait on the first stage runs out (about two seconds).  The kernel must then report
 LR_ERR_TIMEOUT through the status word, release its resources and return, and
 the GPU must stay usable.
 """
-
-import os
 
 import numpy as np
 import pytest
@@ -37,11 +35,11 @@ def test_bounded_wait_reports_timeout_and_gpu_recovers(shape):
     f = dev_factor(21, 0, 0, d_in, d_out, r)
     x_bits = synth.activations(21, M, d_in)
     x = dev_bits(x_bits)
-    os.environ["LR_TEST_STALL_PRODUCER"] = "1"
+    lr.lib.lr_test_stall_producer(1)
     try:
         _, status = _linear(x, f, M)
     finally:
-        del os.environ["LR_TEST_STALL_PRODUCER"]
+        lr.lib.lr_test_stall_producer(0)
     assert status == lr.LR_ERR_TIMEOUT
     # the context is intact: the same call now succeeds and matches the oracle
     y, status = _linear(x, f, M)

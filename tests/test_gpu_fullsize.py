@@ -56,10 +56,16 @@ def test_llama7b_32_layer_graph_step_sampled_rows():
             factors[synth.PROJ_NAMES[p]] = oracle.factor_from_stored(At, Bt)
         hr = oracle.block_forward(hr, factors, m.nh, m.nkv, m.hd)
     assert_parity(h[rows], hr, "7B 32-layer graph step, rows %s" % rows)
+    # the layers' own contribution, without the unit-variance input residual
+    # that dominates rms(h)
+    assert_parity(h[rows] - x, hr - x, "7B 32-layer graph step, h - x0")
 
 
 def _graph_step_rows(model, M, n_layers, rows):
-    """Replay one graph step of the bench workload; return h at `rows` and the oracle's rows."""
+    """Replay one graph step of the bench workload.
+
+    Returns h at `rows`, the oracle's rows and the step's input rows x0.
+    """
     import bench
     w = bench.Workload(torch, lr, M, n_layers, model=model)
     try:
@@ -75,7 +81,8 @@ def _graph_step_rows(model, M, n_layers, rows):
         w.free()
         torch.cuda.empty_cache()
     pool = synth.bf16_normal(0, synth.make_tag(0, 0, synth.KIND_POOL), (pool_rows, model.d), 1.0)
-    hr = oracle.widen_bf16(pool[remap[rows]])
+    x0 = oracle.widen_bf16(pool[remap[rows]])
+    hr = x0
     del pool
     mlp = "relu" if model.mlp == "relu" else "swiglu"
     for layer in range(n_layers):
@@ -87,18 +94,20 @@ def _graph_step_rows(model, M, n_layers, rows):
             At, Bt = synth.factor_pair(0, layer, p, a, b, r)
             factors[synth.PROJ_NAMES[p]] = oracle.factor_from_stored(At, Bt)
         hr = oracle.block_forward(hr, factors, model.nh, model.nkv, model.hd, mlp=mlp)
-    return h, hr
+    return h, hr, x0
 
 
 def test_llama70b_gqa_256_rows_graph_step():
     """70B-GQA shapes (d 8192, ffn 28672, 8 kv heads) at the largest decode batch, 4 layers."""
     import bench
-    h, ref = _graph_step_rows(bench.LLAMA70B, 256, 4, [0, 129, 255])
+    h, ref, x0 = _graph_step_rows(bench.LLAMA70B, 256, 4, [0, 129, 255])
     assert_parity(h, ref, "70B GQA graph step M=256")
+    assert_parity(h - x0, ref - x0, "70B GQA graph step M=256, h - x0")
 
 
 def test_opt30b_relu_64_rows_graph_step():
     """OPT-30B shapes (d 7168, ReLU MLP), 4 layers."""
     import bench
-    h, ref = _graph_step_rows(bench.MODELS["opt30b"], 64, 4, [0, 40, 63])
+    h, ref, x0 = _graph_step_rows(bench.MODELS["opt30b"], 64, 4, [0, 40, 63])
     assert_parity(h, ref, "OPT-30B graph step M=64")
+    assert_parity(h - x0, ref - x0, "OPT-30B graph step M=64, h - x0")

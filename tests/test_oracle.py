@@ -17,6 +17,65 @@ def _bf16_matrix(seed, tag, shape, std=1.0):
     return oracle.widen_bf16(synth.bf16_normal(seed, tag, shape, std))
 
 
+# ----------------------------------------------------------- formats
+def _bf16_by_definition(bits: int) -> Fraction:
+    """Value of a bf16 pattern from its fields: sign, 8-bit biased exponent, 7-bit fraction.
+
+    Written from the format's definition (the top half of an IEEE binary32), with
+    subnormals (exponent field 0) kept exact rather than flushed.
+    """
+    sign = -1 if bits & 0x8000 else 1
+    e = (bits >> 7) & 0xFF
+    m = bits & 0x7F
+    if e == 0:
+        return sign * Fraction(m, 128) * Fraction(1, 2 ** 126)
+    return sign * Fraction(128 + m, 128) * Fraction(2) ** (e - 127)
+
+
+def test_widen_bf16_every_pattern():
+    """widen_bf16 against the exact decoding of all 65,536 bf16 patterns.
+
+    A wrong shift, a lost sign or a flushed subnormal fails here.  Patterns with
+    the exponent field all ones are Inf (fraction 0) or NaN and must map to them.
+    """
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):       # signalling-NaN patterns warn in the fp32 -> fp64 cast
+        got = oracle.widen_bf16(bits)
+    e = (bits >> 7) & 0xFF
+    m = bits & 0x7F
+    special = e == 0xFF
+    assert np.all(np.isinf(got[special & (m == 0)]))
+    assert np.all(np.isnan(got[special & (m != 0)]))
+    finite = np.nonzero(~special)[0]
+    want = np.array([float(_bf16_by_definition(int(b))) for b in finite])
+    assert np.array_equal(got[finite], want)
+    # the sign of zero survives
+    assert np.signbit(got[0x8000]) and not np.signbit(got[0x0000])
+    assert got.dtype == np.float64
+
+
+def test_factor_from_stored_hand_example():
+    """Stored At [r][d_in] and Bt [d_out][r] come back as A_r [d_in][r] and B_r [r][d_out].
+
+    r = 2, d_in = 3, d_out = 4 (no square shape, so a missing transpose fails),
+    with bf16 patterns written out by hand: 1 0x3F80, 2 0x4000, 3 0x4040,
+    4 0x4080, 5 0x40A0, 6 0x40C0, -1 0xBF80, 0.5 0x3F00, -2 0xC000, 0.25 0x3E80.
+    """
+    At = np.array([[0x3F80, 0x4000, 0x4040],            # A_r column 0 = (1, 2, 3)
+                   [0x4080, 0x40A0, 0x40C0]], np.uint16)  # A_r column 1 = (4, 5, 6)
+    Bt = np.array([[0x3F80, 0xBF80],                     # B_r column 0 = (1, -1)
+                   [0x3F00, 0x4000],                     # B_r column 1 = (0.5, 2)
+                   [0x4040, 0x0000],                     # B_r column 2 = (3, 0)
+                   [0xC000, 0x3E80]], np.uint16)         # B_r column 3 = (-2, 0.25)
+    A, B = oracle.factor_from_stored(At, Bt)
+    assert A.shape == (3, 2) and B.shape == (2, 4)
+    assert np.array_equal(A, [[1.0, 4.0], [2.0, 5.0], [3.0, 6.0]])
+    assert np.array_equal(B, [[1.0, 0.5, 3.0, -2.0], [-1.0, 2.0, 0.0, 0.25]])
+    # x = e_0 picks row 0 of A_r B_r: (1, 4) B_r = (1 - 4, 0.5 + 8, 3, -2 + 1)
+    _, y = oracle.lowrank_linear(np.array([[1.0, 0.0, 0.0]]), A, B)
+    assert np.array_equal(y[0], [-3.0, 8.5, 3.0, -1.0])
+
+
 # ----------------------------------------------------------- the linear
 def test_linear_exact_rational_bruteforce():
     """y = (x A) B against exact rational arithmetic on tiny bf16 inputs."""
@@ -261,6 +320,21 @@ def test_remap_out_of_range_and_padding():
     assert np.array_equal(buf[0], pool[3])
     assert not np.any(buf[1]) and not np.any(buf[2])   # bad entries give zero rows
     assert not np.any(buf[3:])                         # rows >= n_active are zero
+
+
+def test_remap_scatter_out_of_range_and_padding():
+    """Out-of-range entries are skipped and flagged; rows at or past n_active are not written."""
+    buf = synth.bf16_normal(0, 81, (5, 4))
+    pool = np.zeros((8, 4), dtype=np.uint16)
+    out, bad = oracle.remap_scatter(buf, [2, 99, -1, 5, 6], 4, pool)
+    assert bad
+    assert np.array_equal(out[2], buf[0]) and np.array_equal(out[5], buf[3])
+    others = [i for i in range(8) if i not in (2, 5)]
+    assert not np.any(out[others])          # 99 and -1 wrote nothing; row 6 is past n_active
+    assert not np.any(pool)                 # the input pool is left alone
+    out, bad = oracle.remap_scatter(buf, [2, 99, -1, 5, 6], 1, pool)
+    assert not bad                          # the bad entries lie past n_active
+    assert np.array_equal(out[2], buf[0]) and np.count_nonzero(np.any(out, axis=1)) <= 1
 
 
 # ----------------------------------------------------- KV reconstruction
