@@ -538,6 +538,63 @@ def rank_sharding(torch, lr, M=64, Gs=(2, 4, 8), rho=RHO, m=None, reps=20):
                                        "their average, not a multi-GPU measurement"}}
 
 
+def decode_sweep(torch, lr, model, n_layers, layers, Ms, steps):
+    """Graph-replayed step time at each decode batch size, the same factors."""
+    out = []
+    for M in Ms:
+        ww = Workload(torch, lr, M, n_layers, seed=0, model=model, layers=layers)
+        ww.stack.capture()
+        t, _ = time_graph(torch, ww.stack, steps, 3)
+        sb = step_bytes(M, n_layers, m=model)
+        out.append({"M": M, "ms_per_step": round(t, 4), "tokens_per_s": round(M / (t * 1e-3), 1),
+                    "step_hbm_gbs": round(sb / (t * 1e-3) / 1e9, 1)})
+        ww.free()
+        del ww
+        torch.cuda.empty_cache()
+    return out
+
+
+def prefill_summary(res, model, M, tf):
+    """Prefill results with named keys: the rho = 0.4 figures at the top, the sweep as a list."""
+    sweep = []
+    for rho, v in sorted(res.items()):
+        v = dict(v)
+        v["rho"] = float(rho)
+        v["frac_of_bf16_peak"] = round(v["tflops"] / tf, 4)
+        sweep.append(v)
+    main = next(v for v in sweep if abs(v["rho"] - 0.4) < 1e-9)
+    return {"workload": "%s-shaped projections of one layer (q,k,v,o,gate,up,down), M=%d rows" % (model.name, M),
+            "M": M, "rho": 0.4, "tflops": main["tflops"], "frac_of_bf16_peak": main["frac_of_bf16_peak"],
+            "ms_per_layer": main["ms_per_layer"],
+            "tokens_per_s_all_layers": main["tokens_per_s_%d_layers" % model.layers],
+            "peak_tflops": tf, "sweep": sweep}
+
+
+def config4(torch, lr, tf, steps):
+    """The LLaMA-70B-GQA-shaped stack (80 layers, rho 0.4): decode sweep and one prefill."""
+    m = LLAMA70B
+    layers = None
+    sweep = []
+    for M in (1, 16, 64, 256):
+        ww = Workload(torch, lr, M, m.layers, seed=0, model=m, layers=layers)
+        layers = ww.layers
+        ww.stack.capture()
+        t, _ = time_graph(torch, ww.stack, steps, 3)
+        sb = step_bytes(M, m.layers, m=m)
+        sweep.append({"M": M, "ms_per_step": round(t, 4), "tokens_per_s": round(M / (t * 1e-3), 1),
+                      "step_hbm_gbs": round(sb / (t * 1e-3) / 1e9, 1)})
+        ww.free()
+        del ww
+        torch.cuda.empty_cache()
+    del layers
+    torch.cuda.empty_cache()
+    pm = 8 * 4096
+    pre = prefill_summary(time_prefill(torch, lr, M=pm, m=m, rhos=(0.4,), reps=2), m, pm, tf)
+    return {"workload": "LLaMA-70B-GQA-shaped 80-layer stack (d 8192, ffn 28672, 8 kv heads, rho 0.4), "
+                        "graph-replayed decode steps; prefill of 8 x 4096 rows through one layer's projections",
+            "layers": m.layers, "decode": sweep, "prefill": pre}
+
+
 def oracle_sample(M, layers_sample, seed=0, rho=RHO, m=LLAMA7B):
     """Time the fp64 oracle on M rows through `layers_sample` layers (factor generation untimed)."""
     import oracle
@@ -615,6 +672,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="0: the model's layer count")
     ap.add_argument("--no-extras", action="store_true", help="skip the M sweep, eager and prefill legs")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--no-config4", action="store_true", help="skip the LLaMA-70B-shaped legs")
     ap.add_argument("--only", choices=["roofline", "prefill"],
                     help="run one leg alone (for profiling): the event-timed decode linears, or "
                          "the prefill projections at rho=0.4")
@@ -705,64 +763,56 @@ def main():
                        "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                        "ms_per_step": round(e2e_s * 1e3, 4),
                        "path": "per step: pinned H2D of remap/n_active, graph replay, D2H of the step's rows, host wait; the host remap_build of the next step overlaps the GPU work"}
-        r = time_linears(torch, lr, w)
-        nl = r["launches"]
-        achieved = r["bytes"] / r["chained_s"] / 1e9
+        # Roofline of the step as it runs: the graph's own launches, timed by
+        # the CUDA events of the timed region above.  The algorithmic bytes are
+        # the factors plus every linear's x in and y out; the glue kernels'
+        # time is included, so this is a lower bound for the GEMM kernel alone.
+        per_step = w.stack.launch_count()
+        sb = step_bytes(args.M, args.layers, m=model)
+        achieved = sb / (ms * 1e-3) / 1e9
         traffic = decode_traffic() if model.name == "llama7b" and args.M == 64 else None
         line["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                             "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": peak_kind,
-                            "kernel": "decode_kernel (tcgen05 swap-AB): the down and up launches of every "
-                                      "linear of the stack, back to back in one CUDA graph",
-                            "launches_timed": nl, "avg_launch_us": round(r["chained_s"] / nl * 1e6, 2),
-                            "algorithmic_bytes_per_launch": round(r["bytes"] / nl),
-                            "isolated": {"achieved": round(r["bytes"] / r["isolated_s"] / 1e9, 1),
-                                         "avg_launch_us": round(r["isolated_s"] / nl * 1e6, 2),
-                                         "note": "each linear timed alone with an event pair",
-                                         "per_projection_gbs": r["isolated_per_projection_gbs"]}}
+                            "kernel": "decode_kernel (tcgen05 swap-AB down/up projections) with the step's "
+                                      "glue kernels, as replayed in the step's CUDA graph",
+                            "timed": "CUDA events around the timed replays on the replay stream",
+                            "launches_timed": per_step * args.steps,
+                            "avg_launch_us": round(ms * 1e3 / per_step, 3),
+                            "algorithmic_bytes_per_step": sb,
+                            "algorithmic_bytes_per_launch": round(sb / per_step)}
         if not args.no_extras:
+            r = time_linears(torch, lr, w)
+            line["roofline"]["isolated_linears"] = {
+                "achieved": round(r["bytes"] / r["isolated_s"] / 1e9, 1),
+                "avg_launch_us": round(r["isolated_s"] / r["launches"] * 1e6, 2),
+                "note": "each linear of the stack (down + up launch) timed alone with an event pair",
+                "per_projection_gbs": r["isolated_per_projection_gbs"]}
             # the analogue of the pages' CUDA-graph ablation: the same step
-            # replayed as a graph, enqueued eagerly, and as one persistent kernel
+            # replayed as a graph and enqueued eagerly
             eager_ms = time_eager(torch, w.stack, 5, 3)
             cmp = {"graph_ms": round(ms, 4), "eager_ms": round(eager_ms, 4),
                    "launches_per_step": w.stack.launch_count()}
-            if model.mlp == "swiglu":   # the persistent step runs SiLU-GLU blocks only
-                w.stack.destroy()
-                w.stack.mode = lr.STACK_PERSISTENT
-                w.stack._desc = None
-                need = lr.Stack.scratch_bytes(args.M, w.layers, lr.STACK_PERSISTENT)
-                w.stack.scratch = torch.zeros(need, dtype=torch.uint8, device="cuda")
-                w.stack.capture()
-                pers_ms, _ = time_graph(torch, w.stack, 10, 3)
-                cmp["persistent_graph_ms"] = round(pers_ms, 4)
             line["graph_vs_eager"] = cmp
         layers = w.layers
         w.free()
         del w
         torch.cuda.empty_cache()
         if not args.no_extras:
-            sweep = {}
-            for M in ((1, 8, 32, 64) if model.name != "llama70b" else (1, 16, 64, 256)):
-                ww = Workload(torch, lr, M, args.layers, seed=0, model=model, layers=layers)
-                ww.stack.capture()
-                t, _ = time_graph(torch, ww.stack, max(10, args.steps // 2), 3)
-                sweep[str(M)] = {"ms_per_step": round(t, 4), "tokens_per_s": round(M / (t * 1e-3), 1),
-                                 "step_hbm_gbs": round(step_bytes(M, args.layers, m=model) / (t * 1e-3) / 1e9, 1)}
-                ww.free()
-                del ww
-                torch.cuda.empty_cache()
-            line["decode_sweep"] = sweep
+            line["decode_sweep"] = decode_sweep(torch, lr, model, args.layers, layers,
+                                                (1, 8, 32, 64) if model.name != "llama70b" else (1, 16, 64, 256),
+                                                max(10, args.steps // 2))
             del layers
             torch.cuda.empty_cache()
-            if model.name == "llama7b":
-                pre = time_prefill(torch, lr)
-            else:
-                pre = time_prefill(torch, lr, M=8 * 4096 if model.name == "llama70b" else 16384,
-                                   rhos=(0.4,), m=model)
-            for v in pre.values():
-                v["frac_of_bf16_peak"] = round(v["tflops"] / tf, 4)
-            line["prefill"] = pre
+            pm = 8 * 4096 if model.name == "llama70b" else 16384
+            line["prefill"] = prefill_summary(time_prefill(torch, lr, M=pm, m=model,
+                                                           rhos=(0.2, 0.4, 0.6) if model.name == "llama7b" else (0.4,)),
+                                              model, pm, tf)
             line["kv_reconstruct"] = time_kv_reconstruct(torch, lr, m=model)
             line["rank_sharding"] = rank_sharding(torch, lr)
+            if model.name == "llama7b" and not args.no_config4:
+                line["config4"] = config4(torch, lr, tf, max(10, args.steps // 2))
+        else:
+            del layers
         if not args.no_cpu:
             sample_layers = oracle_sample_layers(args.layers)
             tcpu, n = oracle_sample(args.M, sample_layers, m=model)

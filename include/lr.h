@@ -75,6 +75,18 @@ typedef struct {
   int32_t r;
 } lr_factor;
 
+/* lr_factor_pack: the factors in the pages' orientation, W ~ A_r B_r
+ * (Spanish page, "Resumen Tecnico" section 1), to the layout above.
+ *   A: device bf16 [d_in][r] row-major (A_r);  B: device bf16 [r][d_out]
+ *   row-major (B_r).  At: device bf16 [r][d_in], Bt: device bf16 [d_out][r],
+ *   written as the exact transposes (bit-for-bit copies of every element).
+ *   d_in, d_out, r positive multiples of 64 (LR_ERR_UNSUPPORTED otherwise);
+ *   every pointer 16-byte aligned; the four buffers must not overlap
+ *   (LR_ERR_INVALID_ARG).  Enqueued on s; a one-time step when a model's
+ *   factors are loaded, not part of a decode step. */
+lr_status lr_factor_pack(const void* A, const void* B, int32_t d_in, int32_t d_out, int32_t r, void* At,
+                         void* Bt, lr_stream s);
+
 /* Projections of a block, in this order (English page section 2.D: attention
  * and MLP projections are all decomposed). */
 enum { LR_Q = 0, LR_K = 1, LR_V = 2, LR_O = 3, LR_GATE = 4, LR_UP = 5, LR_DOWN = 6 };
@@ -274,7 +286,7 @@ lr_status lr_rank_shard_comm_bytes(int64_t M, int32_t d_out, int32_t r, int32_t 
  * scratch: max over layers of lr_block_scratch_bytes(cap, layer).
  * All layers must share d_model.  Rows i >= *n_active run through the layers
  * as zero rows and are not scattered. */
-enum { LR_STACK_AUTO = 0, LR_STACK_LAYERED = 1, LR_STACK_PERSISTENT = 2 };
+enum { LR_STACK_AUTO = 0, LR_STACK_LAYERED = 1 };
 typedef struct {
   int32_t n_layers;
   const lr_block_desc* layers; /* host array [n_layers]; copied by the calls */
@@ -290,21 +302,19 @@ typedef struct {
   void* scratch;
   size_t scratch_bytes;
   int32_t* dev_status;
-  /* LR_STACK_AUTO / LR_STACK_LAYERED: one launch per kernel, chained by
-   * programmatic dependent launch.  LR_STACK_PERSISTENT (cap <= 256): the
-   * whole step as one cooperative kernel, one CTA per SM walking a program
-   * of phases separated by grid barriers. */
+  /* LR_STACK_AUTO (= LR_STACK_LAYERED): one launch per kernel, chained by
+   * programmatic dependent launch.  Other values are rejected
+   * (LR_ERR_INVALID_ARG). */
   int32_t mode;
 } lr_stack_desc;
 
-/* Scratch the step needs: the block buffers plus, in persistent mode, the
- * step's program (tensor maps, phases, work segments), split-K partials and
- * counters.  Uses only n_layers, layers, cap and mode of the descriptor.
- * A captured graph keeps using its scratch until lr_graph_destroy. */
+/* Scratch the step needs: the block buffers of the largest layer (layers run
+ * one after another and reuse them).  Uses only n_layers, layers and cap of
+ * the descriptor.  A captured graph keeps using its scratch until
+ * lr_graph_destroy. */
 size_t lr_stack_scratch_bytes(const lr_stack_desc* st);
 
-/* Enqueue one step eagerly.  In persistent mode the program is rebuilt and
- * copied to the scratch first (the call waits for that copy on stream s). */
+/* Enqueue one step eagerly on stream s. */
 lr_status lr_stack_forward(const lr_stack_desc* st, lr_stream s);
 
 /* Capture one step into a CUDA graph owned by the library (captured on a
@@ -316,8 +326,7 @@ lr_status lr_graph_capture(const lr_stack_desc* st, lr_graph** out);
 lr_status lr_graph_replay(lr_graph* g, lr_stream s);
 lr_status lr_graph_destroy(lr_graph* g);
 
-/* Number of kernel launches one step enqueues (eager or in the graph):
- * 1 in persistent mode. */
+/* Number of kernel launches one step enqueues (eager or in the graph). */
 int64_t lr_stack_launch_count(const lr_stack_desc* st);
 
 const char* lr_status_string(lr_status st);
@@ -333,6 +342,7 @@ const char* lr_last_error(void);
  * failure-detection tests only; nothing else sets it, and no environment
  * variable does. */
 void lr_test_stall_producer(int32_t on);
+
 
 #ifdef __cplusplus
 }

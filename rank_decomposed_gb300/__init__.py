@@ -64,7 +64,6 @@ class StackDesc(ctypes.Structure):
 
 STACK_AUTO = 0
 STACK_LAYERED = 1
-STACK_PERSISTENT = 2
 
 
 def _load():
@@ -78,6 +77,7 @@ def _load():
         "lr_linear_workspace_bytes": (sz, [i64, P(Factor)]),
         "lr_linear_forward": (i32, [vp, i64, vp, i64, i32, i64, P(Factor), vp, sz, vp, vp]),
         "lr_linear_forward_noalloc": (i32, [vp, i64, vp, i64, i32, i64, P(Factor), vp, vp]),
+        "lr_factor_pack": (i32, [vp, vp, i32, i32, i32, vp, vp, vp]),
         "lr_block_scratch_bytes": (sz, [i64, P(BlockDesc)]),
         "lr_block_forward": (i32, [vp, i64, P(BlockDesc), vp, sz, vp, vp]),
         "remap_compact": (i32, [vp, i64, i64, vp, vp, vp, i64, vp, vp]),
@@ -188,6 +188,27 @@ class Block:
             if f is not None:
                 b.f[i] = f.c()
         return b
+
+
+def factor_pack(A, B, stream=None) -> FactorPair:
+    """A FactorPair from the pages' orientation: A_r bf16 [d_in][r], B_r bf16 [r][d_out] (device).
+
+    The library stores the transposes (At = A_r^T, Bt = B_r^T); lr_factor_pack
+    writes them on the device.  Allocation of the two outputs is done here
+    with torch.
+    """
+    import torch
+    _bf16(A, "A")
+    _bf16(B, "B")
+    if A.shape[1] != B.shape[0]:
+        raise ValueError("A [d_in][r] and B [r][d_out] disagree on r")
+    d_in, r = A.shape
+    d_out = B.shape[1]
+    At = torch.empty((r, d_in), dtype=torch.bfloat16, device=A.device)
+    Bt = torch.empty((d_out, r), dtype=torch.bfloat16, device=B.device)
+    _check("lr_factor_pack", lib.lr_factor_pack(A.data_ptr(), B.data_ptr(), d_in, d_out, r, At.data_ptr(),
+                                                Bt.data_ptr(), _stream(stream)))
+    return FactorPair(At, Bt)
 
 
 # --------------------------------------------------------------- linear
@@ -374,7 +395,7 @@ class Stack:
 
     @staticmethod
     def scratch_bytes(cap: int, layers, mode: int = STACK_AUTO) -> int:
-        """Scratch bytes of a step over `cap` rows (block buffers + persistent program)."""
+        """Scratch bytes of a step over `cap` rows (the block buffers)."""
         arr = (BlockDesc * len(layers))(*[b.c() for b in layers])
         d = StackDesc()
         d.n_layers = len(layers)

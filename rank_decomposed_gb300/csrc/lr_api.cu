@@ -118,8 +118,6 @@ lr_status ensure_configured() {
   if (st != LR_OK) return st;
   st = configure_prefill();
   if (st != LR_OK) return st;
-  st = configure_persist();
-  if (st != LR_OK) return st;
   done[dev] = true;
   return LR_OK;
 }
@@ -204,13 +202,7 @@ lr_status enqueue_linear(const void* x, int64_t ldx, void* y, int64_t ldy, lr_dt
   return run_ops(M, &up, 1, status, s);
 }
 
-namespace {
-
 // ---------------------------------------------------------------- block
-struct BlockLayout {
-  size_t n1, t[7], q, k, v, n2, g, u, a, total;
-};
-
 BlockLayout block_layout(int64_t M, const lr_block_desc* b) {
   BlockLayout L;
   size_t off = 0;
@@ -235,6 +227,8 @@ BlockLayout block_layout(int64_t M, const lr_block_desc* b) {
   L.total = off;
   return L;
 }
+
+namespace {
 
 lr_status check_block(const lr_block_desc* b) {
   if (b == nullptr) return invalid("block: null descriptor");
@@ -268,33 +262,55 @@ lr_status check_block(const lr_block_desc* b) {
   return LR_OK;
 }
 
-lr_status enqueue_block(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws,
-                        int32_t* status, cudaStream_t s) {
+// One launch of a block, in stream order: a GEMM group (ops sharing M and
+// their input), an RMSNorm or a SiLU-GLU.
+struct Step {
+  enum Kind { GEMM, RMSNORM, SILU } kind;
+  GemmOp ops[kMaxGroup];
+  int n = 0;
+  const void* src0 = nullptr;
+  const void* src1 = nullptr;
+  void* dst = nullptr;
+  int d = 0;
+  float eps = 0.f;
+};
+
+Step gemm_step(std::initializer_list<GemmOp> ops) {
+  Step st;
+  st.kind = Step::GEMM;
+  for (const GemmOp& o : ops) st.ops[st.n++] = o;
+  return st;
+}
+
+// The launches of one block: n1 = RMSNorm(h); q, k, v = LR(n1) (down group,
+// then up group); h += LR_o(attn(v)); n2 = RMSNorm(h);
+// h += LR_down(silu(LR_gate(n2)) * LR_up(n2)) (ReLU variant: the ReLU is
+// applied in the up projection's epilogue).
+void block_steps(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws, std::vector<Step>& out) {
   const BlockLayout L = block_layout(M, b);
   const int d = b->d_model, dff = b->d_ff;
   const lr_factor* f = b->f;
   void* t[7];
   for (int i = 0; i < 7; ++i) t[i] = ws + L.t[i];
-  void* n1 = ws + L.n1;
-  void* n2 = ws + L.n2;
-  lr_status st;
-#define LR_TRY(x)          \
-  do {                     \
-    st = (x);              \
-    if (st != LR_OK) return st; \
-  } while (0)
-  // attention half: n1 = RMSNorm(h); q, k, v = LR(n1); h += LR_o(attn(v))
-  LR_TRY(launch_rmsnorm(h, n1, M, d, b->eps, s));
+  Step norm;
+  norm.kind = Step::RMSNORM;
+  norm.src0 = h;
+  norm.dst = ws + L.n1;
+  norm.d = d;
+  norm.eps = b->eps;
+  out.push_back(norm);
   {
-    GemmOp down[3], up[3];
     void* outs[3] = {ws + L.q, ws + L.k, ws + L.v};
+    Step dn, up;
+    dn.kind = up.kind = Step::GEMM;
     for (int i = 0; i < 3; ++i) {
-      down[i] = make_op(f[i].At, f[i].r, d, n1, d, d, EPI_STORE_BF16, t[i], f[i].r);
-      up[i] = make_op(f[i].Bt, f[i].d_out, f[i].r, t[i], f[i].r, f[i].r, EPI_STORE_BF16, outs[i],
-                      f[i].d_out);
+      dn.ops[i] = make_op(f[i].At, f[i].r, d, ws + L.n1, d, d, EPI_STORE_BF16, t[i], f[i].r);
+      up.ops[i] = make_op(f[i].Bt, f[i].d_out, f[i].r, t[i], f[i].r, f[i].r, EPI_STORE_BF16, outs[i],
+                          f[i].d_out);
     }
-    LR_TRY(run_ops(M, down, 3, status, s));
-    LR_TRY(run_ops(M, up, 3, status, s));
+    dn.n = up.n = 3;
+    out.push_back(dn);
+    out.push_back(up);
   }
   {
     const int dq = b->n_heads * b->head_dim, dkv = b->n_kv_heads * b->head_dim;
@@ -304,40 +320,63 @@ lr_status enqueue_block(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws
       od.gqa_head_dim = b->head_dim;
       od.gqa_group = b->n_heads / b->n_kv_heads;
     }
-    GemmOp ou = make_op(f[LR_O].Bt, d, f[LR_O].r, t[LR_O], f[LR_O].r, f[LR_O].r, EPI_ADD_F32, h, d);
-    LR_TRY(run_ops(M, &od, 1, status, s));
-    LR_TRY(run_ops(M, &ou, 1, status, s));
+    out.push_back(gemm_step({od}));
+    out.push_back(gemm_step(
+        {make_op(f[LR_O].Bt, d, f[LR_O].r, t[LR_O], f[LR_O].r, f[LR_O].r, EPI_ADD_F32, h, d)}));
   }
-  // MLP half: n2 = RMSNorm(h); h += LR_down(silu(LR_gate(n2)) * LR_up(n2))
-  LR_TRY(launch_rmsnorm(h, n2, M, d, b->eps, s));
+  norm.dst = ws + L.n2;
+  out.push_back(norm);
   if (b->mlp == LR_MLP_SWIGLU) {
-    GemmOp down[2], up[2];
     void* outs[2] = {ws + L.g, ws + L.u};
+    Step dn, up;
+    dn.kind = up.kind = Step::GEMM;
     for (int i = 0; i < 2; ++i) {
       const lr_factor& fi = f[LR_GATE + i];
-      down[i] = make_op(fi.At, fi.r, d, n2, d, d, EPI_STORE_BF16, t[LR_GATE + i], fi.r);
-      up[i] = make_op(fi.Bt, dff, fi.r, t[LR_GATE + i], fi.r, fi.r, EPI_STORE_BF16, outs[i], dff);
+      dn.ops[i] = make_op(fi.At, fi.r, d, ws + L.n2, d, d, EPI_STORE_BF16, t[LR_GATE + i], fi.r);
+      up.ops[i] = make_op(fi.Bt, dff, fi.r, t[LR_GATE + i], fi.r, fi.r, EPI_STORE_BF16, outs[i], dff);
     }
-    LR_TRY(run_ops(M, down, 2, status, s));
-    LR_TRY(run_ops(M, up, 2, status, s));
-    LR_TRY(launch_silu_mul(ws + L.g, ws + L.u, ws + L.a, M, dff, s));
+    dn.n = up.n = 2;
+    out.push_back(dn);
+    out.push_back(up);
+    Step act;
+    act.kind = Step::SILU;
+    act.src0 = ws + L.g;
+    act.src1 = ws + L.u;
+    act.dst = ws + L.a;
+    act.d = dff;
+    out.push_back(act);
   } else {
-    // non-GLU: a = relu(LR_up(n2)), the ReLU applied in the GEMM's epilogue
     const lr_factor& fu = f[LR_UP];
-    GemmOp ud = make_op(fu.At, fu.r, d, n2, d, d, EPI_STORE_BF16, t[LR_UP], fu.r);
-    GemmOp uu = make_op(fu.Bt, dff, fu.r, t[LR_UP], fu.r, fu.r, EPI_RELU_BF16, ws + L.a, dff);
-    LR_TRY(run_ops(M, &ud, 1, status, s));
-    LR_TRY(run_ops(M, &uu, 1, status, s));
+    out.push_back(gemm_step({make_op(fu.At, fu.r, d, ws + L.n2, d, d, EPI_STORE_BF16, t[LR_UP], fu.r)}));
+    out.push_back(gemm_step({make_op(fu.Bt, dff, fu.r, t[LR_UP], fu.r, fu.r, EPI_RELU_BF16, ws + L.a, dff)}));
   }
-  {
-    const lr_factor& fd = f[LR_DOWN];
-    GemmOp dd = make_op(fd.At, fd.r, dff, ws + L.a, dff, dff, EPI_STORE_BF16, t[LR_DOWN], fd.r);
-    GemmOp du = make_op(fd.Bt, d, fd.r, t[LR_DOWN], fd.r, fd.r, EPI_ADD_F32, h, d);
-    LR_TRY(run_ops(M, &dd, 1, status, s));
-    LR_TRY(run_ops(M, &du, 1, status, s));
+  const lr_factor& fd = f[LR_DOWN];
+  out.push_back(gemm_step({make_op(fd.At, fd.r, dff, ws + L.a, dff, dff, EPI_STORE_BF16, t[LR_DOWN], fd.r)}));
+  out.push_back(gemm_step({make_op(fd.Bt, d, fd.r, t[LR_DOWN], fd.r, fd.r, EPI_ADD_F32, h, d)}));
+}
+
+// Enqueue steps in order.
+lr_status enqueue_steps(const std::vector<Step>& steps, int64_t M, int32_t* status, cudaStream_t s) {
+  for (size_t i = 0; i < steps.size(); ++i) {
+    const Step& st = steps[i];
+    lr_status r;
+    if (st.kind == Step::GEMM) {
+      r = run_ops(M, st.ops, st.n, status, s);
+    } else if (st.kind == Step::RMSNORM) {
+      r = launch_rmsnorm(static_cast<const float*>(st.src0), st.dst, M, st.d, st.eps, s);
+    } else {
+      r = launch_silu_mul(st.src0, st.src1, st.dst, M, st.d, s);
+    }
+    if (r != LR_OK) return r;
   }
-#undef LR_TRY
   return LR_OK;
+}
+
+lr_status enqueue_block(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws,
+                        int32_t* status, cudaStream_t s) {
+  std::vector<Step> steps;
+  block_steps(h, M, b, ws, steps);
+  return enqueue_steps(steps, M, status, s);
 }
 
 int64_t block_launches(int64_t M, const lr_block_desc* b) {
@@ -349,264 +388,11 @@ int64_t block_launches(int64_t M, const lr_block_desc* b) {
 }
 
 // ---------------------------------------------------------------- stack
-bool use_persist(const lr_stack_desc* st) {
-  return st->mode == LR_STACK_PERSISTENT && st->cap <= persist_max_rows();
-}
-
 size_t block_region_bytes(const lr_stack_desc* st) {
   size_t need = 0;
   for (int l = 0; l < st->n_layers; ++l)
     need = std::max(need, block_layout(st->cap, &st->layers[l]).total);
   return align_up(need);
-}
-
-// Weight tiles (16 KB each) a CTA keeps requested into L2 beyond its shared-
-// memory ring.  152 CTAs x 32 tiles = 78 MB in flight or resident in L2.
-int persist_prefetch_tiles() {
-  static const int v = [] {
-    const char* e = getenv("LR_PERSIST_PREFETCH");
-    return (e && *e) ? atoi(e) : 32;
-  }();
-  return v;
-}
-
-int pick_nt(int64_t cap) {
-  return cap <= 16 ? 16 : cap <= 32 ? 32 : cap <= 64 ? 64 : cap <= 128 ? 128 : 256;
-}
-
-// Host-side program of the persistent decode step (see lr_persist.cu).
-struct MapReq {
-  const void* ptr;
-  uint64_t rows, cols, ld;
-  uint32_t box_rows;
-};
-
-struct Plan {
-  int G = 0, nt = 0, M = 0;
-  std::vector<PPhase> phases;
-  std::vector<PProblem> probs;
-  std::vector<MapReq> maps;
-  std::vector<std::vector<PSeg>> per_cta;
-  int n_ctr = 0;
-  int max_slots = 0;
-  // layout of the persistent region
-  size_t off_maps = 0, off_phases = 0, off_probs = 0, off_segs = 0, off_begin = 0;
-  size_t off_partials = 0, off_zero = 0, zero_bytes = 0, total = 0, n_segs = 0;
-};
-
-int add_map(Plan& P, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box) {
-  P.maps.push_back(MapReq{ptr, rows, cols, ld, box});
-  return static_cast<int>(P.maps.size()) - 1;
-}
-
-void add_glue(Plan& P, int kind, int d, const void* s0, const void* s1, void* d0, void* d1,
-              float eps) {
-  PPhase ph;
-  memset(&ph, 0, sizeof(ph));
-  ph.kind = kind;
-  ph.d = d;
-  ph.src0 = s0;
-  ph.src1 = s1;
-  ph.dst0 = d0;
-  ph.dst1 = d1;
-  ph.eps = eps;
-  P.phases.push_back(ph);
-}
-
-// A GEMM phase: its (tile, k-block) units are dealt out stream-K style, CTA c
-// taking units [c U / G, (c + 1) U / G).
-void add_gemm(Plan& P, const GemmOp* ops, int n_ops) {
-  const int phase = static_cast<int>(P.phases.size());
-  add_glue(P, PH_GEMM, 0, nullptr, nullptr, nullptr, nullptr, 0.f);
-  const int prob0 = static_cast<int>(P.probs.size());
-  std::vector<int64_t> ubase(n_ops + 1, 0);
-  std::vector<int> tiles(n_ops), nkb(n_ops);
-  for (int g = 0; g < n_ops; ++g) {
-    const GemmOp& o = ops[g];
-    PProblem pr;
-    memset(&pr, 0, sizeof(pr));
-    pr.wmap = add_map(P, o.W, o.N, o.K, o.ldw, 128);
-    pr.amap = add_map(P, o.act, P.M, o.act_cols, o.ld_act, P.nt);
-    pr.N = o.N;
-    pr.nkb = o.K / 64;
-    pr.epi = o.epi;
-    pr.vec_ok = (reinterpret_cast<uintptr_t>(o.out) % 16 == 0) && (o.ldo % 8 == 0) ? 1 : 0;
-    pr.gqa_head_dim = o.gqa_head_dim;
-    pr.gqa_group = o.gqa_group;
-    pr.out = o.out;
-    pr.ldo = o.ldo;
-    P.probs.push_back(pr);
-    tiles[g] = (o.N + 127) / 128;
-    nkb[g] = pr.nkb;
-    ubase[g + 1] = ubase[g] + static_cast<int64_t>(tiles[g]) * nkb[g];
-  }
-  const int64_t U = ubase[n_ops];
-  // contributors of every tile: (cta, index of the segment in that CTA's list)
-  std::vector<std::vector<std::pair<int, int>>> contrib;
-  std::vector<int64_t> tile_base(n_ops + 1, 0);
-  for (int g = 0; g < n_ops; ++g) tile_base[g + 1] = tile_base[g] + tiles[g];
-  contrib.resize(tile_base[n_ops]);
-  for (int c = 0; c < P.G; ++c) {
-    int64_t u = U * c / P.G;
-    const int64_t u1 = U * (c + 1) / P.G;
-    while (u < u1) {
-      int g = 0;
-      while (ubase[g + 1] <= u) ++g;
-      const int64_t lu = u - ubase[g];
-      const int tile = static_cast<int>(lu / nkb[g]);
-      const int kb0 = static_cast<int>(lu % nkb[g]);
-      const int64_t tile_end = ubase[g] + static_cast<int64_t>(tile + 1) * nkb[g];
-      const int64_t e = std::min(u1, tile_end);
-      PSeg sg;
-      memset(&sg, 0, sizeof(sg));
-      sg.phase = phase;
-      sg.prob = prob0 + g;
-      sg.tile = tile;
-      sg.kb0 = kb0;
-      sg.kb1 = kb0 + static_cast<int>(e - u);
-      sg.nc = 1;
-      contrib[tile_base[g] + tile].push_back({c, static_cast<int>(P.per_cta[c].size())});
-      P.per_cta[c].push_back(sg);
-      u = e;
-    }
-  }
-  int slots = 0;
-  for (auto& list : contrib) {
-    const int nc = static_cast<int>(list.size());
-    if (nc <= 1) continue;
-    const int ctr = P.n_ctr++;
-    for (int j = 0; j < nc; ++j) {
-      PSeg& sg = P.per_cta[list[j].first][list[j].second];
-      sg.j = j;
-      sg.nc = nc;
-      sg.slot = slots;
-      sg.ctr = ctr;
-    }
-    slots += nc;
-  }
-  P.max_slots = std::max(P.max_slots, slots);
-}
-
-// Builds the phase program of one decode step over the stack's fixed buffers.
-void build_plan(const lr_stack_desc* st, Plan& P) {
-  P.G = persist_grid();
-  P.M = static_cast<int>(st->cap);
-  P.nt = pick_nt(st->cap);
-  P.per_cta.assign(P.G, {});
-  const int d = st->layers[0].d_model;
-  uint8_t* ws = static_cast<uint8_t*>(st->scratch);
-  float* h = st->h;
-  add_glue(P, PH_GATHER, d, st->pool_in, nullptr, h, st->xbuf, 0.f);
-  for (int l = 0; l < st->n_layers; ++l) {
-    const lr_block_desc* b = &st->layers[l];
-    const BlockLayout L = block_layout(st->cap, b);
-    const lr_factor* f = b->f;
-    const int dff = b->d_ff;
-    void* t[7];
-    for (int i = 0; i < 7; ++i) t[i] = ws + L.t[i];
-    add_glue(P, PH_RMSNORM, d, h, nullptr, ws + L.n1, nullptr, b->eps);
-    GemmOp down[3], up[3];
-    void* outs[3] = {ws + L.q, ws + L.k, ws + L.v};
-    for (int i = 0; i < 3; ++i) {
-      down[i] = make_op(f[i].At, f[i].r, d, ws + L.n1, d, d, EPI_STORE_BF16, t[i], f[i].r);
-      up[i] = make_op(f[i].Bt, f[i].d_out, f[i].r, t[i], f[i].r, f[i].r, EPI_STORE_BF16, outs[i],
-                      f[i].d_out);
-    }
-    add_gemm(P, down, 3);
-    add_gemm(P, up, 3);
-    const int dq = b->n_heads * b->head_dim, dkv = b->n_kv_heads * b->head_dim;
-    GemmOp od = make_op(f[LR_O].At, f[LR_O].r, dq, ws + L.v, dkv, dkv, EPI_STORE_BF16, t[LR_O],
-                        f[LR_O].r);
-    if (b->n_heads != b->n_kv_heads) {
-      od.gqa_head_dim = b->head_dim;
-      od.gqa_group = b->n_heads / b->n_kv_heads;
-    }
-    GemmOp ou = make_op(f[LR_O].Bt, d, f[LR_O].r, t[LR_O], f[LR_O].r, f[LR_O].r, EPI_ADD_F32, h, d);
-    add_gemm(P, &od, 1);
-    add_gemm(P, &ou, 1);
-    add_glue(P, PH_RMSNORM, d, h, nullptr, ws + L.n2, nullptr, b->eps);
-    GemmOp gd[2], gu[2];
-    void* gouts[2] = {ws + L.g, ws + L.u};
-    for (int i = 0; i < 2; ++i) {
-      const lr_factor& fi = f[LR_GATE + i];
-      gd[i] = make_op(fi.At, fi.r, d, ws + L.n2, d, d, EPI_STORE_BF16, t[LR_GATE + i], fi.r);
-      gu[i] = make_op(fi.Bt, dff, fi.r, t[LR_GATE + i], fi.r, fi.r, EPI_STORE_BF16, gouts[i], dff);
-    }
-    add_gemm(P, gd, 2);
-    add_gemm(P, gu, 2);
-    add_glue(P, PH_SILU, dff, ws + L.g, ws + L.u, ws + L.a, nullptr, 0.f);
-    const lr_factor& fd = f[LR_DOWN];
-    GemmOp dd = make_op(fd.At, fd.r, dff, ws + L.a, dff, dff, EPI_STORE_BF16, t[LR_DOWN], fd.r);
-    GemmOp du = make_op(fd.Bt, d, fd.r, t[LR_DOWN], fd.r, fd.r, EPI_ADD_F32, h, d);
-    add_gemm(P, &dd, 1);
-    add_gemm(P, &du, 1);
-  }
-  add_glue(P, PH_SCATTER, d, h, nullptr, st->pool_out, st->ybuf, 0.f);
-
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    const size_t o = off;
-    off = align_up(off + bytes);
-    return o;
-  };
-  P.n_segs = 0;
-  for (auto& v : P.per_cta) P.n_segs += v.size();
-  P.off_maps = take(P.maps.size() * sizeof(CUtensorMap));
-  P.off_phases = take(P.phases.size() * sizeof(PPhase));
-  P.off_probs = take(P.probs.size() * sizeof(PProblem));
-  P.off_segs = take(P.n_segs * sizeof(PSeg));
-  P.off_begin = take((P.G + 1) * sizeof(int32_t));
-  P.off_partials = take(static_cast<size_t>(std::max(P.max_slots, 1)) * P.nt * 128 * sizeof(float));
-  P.off_zero = off;
-  P.zero_bytes = align_up((P.n_ctr + 2) * sizeof(uint32_t));
-  P.total = P.off_zero + P.zero_bytes;
-}
-
-// Encodes the tensor maps and copies the program into the persistent region;
-// returns the kernel's parameters.  Ordered on stream `s`, and complete on
-// return.
-lr_status upload_plan(const lr_stack_desc* st, Plan& P, cudaStream_t s, PersistParams* out) {
-  uint8_t* region = static_cast<uint8_t*>(st->scratch) + block_region_bytes(st);
-  std::vector<uint8_t> host(P.off_partials, 0);
-  CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(host.data() + P.off_maps);
-  for (size_t i = 0; i < P.maps.size(); ++i) {
-    const MapReq& m = P.maps[i];
-    lr_status r = encode_map_bf16(&maps[i], m.ptr, m.rows, m.cols, m.ld, m.box_rows);
-    if (r != LR_OK) return r;
-  }
-  memcpy(host.data() + P.off_phases, P.phases.data(), P.phases.size() * sizeof(PPhase));
-  memcpy(host.data() + P.off_probs, P.probs.data(), P.probs.size() * sizeof(PProblem));
-  PSeg* segs = reinterpret_cast<PSeg*>(host.data() + P.off_segs);
-  int32_t* begin = reinterpret_cast<int32_t*>(host.data() + P.off_begin);
-  size_t k = 0;
-  for (int c = 0; c < P.G; ++c) {
-    begin[c] = static_cast<int32_t>(k);
-    for (const PSeg& sg : P.per_cta[c]) segs[k++] = sg;
-  }
-  begin[P.G] = static_cast<int32_t>(k);
-  cudaError_t e = cudaMemcpyAsync(region, host.data(), host.size(), cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return cuda_fail(e, "stack: upload program");
-  PersistParams& p = *out;
-  memset(&p, 0, sizeof(p));
-  p.M = P.M;
-  p.G = P.G;
-  p.n_phases = static_cast<int32_t>(P.phases.size());
-  p.pf_ahead = persist_prefetch_tiles();
-  p.phases = reinterpret_cast<const PPhase*>(region + P.off_phases);
-  p.probs = reinterpret_cast<const PProblem*>(region + P.off_probs);
-  p.segs = reinterpret_cast<const PSeg*>(region + P.off_segs);
-  p.seg_begin = reinterpret_cast<const int32_t*>(region + P.off_begin);
-  p.maps = reinterpret_cast<const CUtensorMap*>(region + P.off_maps);
-  p.partials = reinterpret_cast<float*>(region + P.off_partials);
-  p.counters = reinterpret_cast<uint32_t*>(region + P.off_zero);
-  p.gbar = p.counters + P.n_ctr;
-  p.abort_flag = reinterpret_cast<int32_t*>(p.gbar + 1);
-  p.status = st->dev_status;
-  p.remap = st->remap;
-  p.n_active = st->n_active;
-  p.pool_rows = st->pool_rows;
-  return LR_OK;
 }
 
 lr_status check_stack(const lr_stack_desc* st) {
@@ -615,16 +401,7 @@ lr_status check_stack(const lr_stack_desc* st) {
     return invalid("stack: bad layer array");
   if (st->n_layers == 0) return invalid("stack: no layers");
   if (st->cap <= 0 || st->cap > kDecodeMaxRows * 64) return invalid("stack: bad cap");
-  if (st->mode != LR_STACK_AUTO && st->mode != LR_STACK_LAYERED && st->mode != LR_STACK_PERSISTENT)
-    return invalid("stack: bad mode");
-  if (st->mode == LR_STACK_PERSISTENT && st->cap > persist_max_rows())
-    return invalid("stack: the persistent step takes at most %d rows", persist_max_rows());
-  if (st->mode == LR_STACK_PERSISTENT)
-    for (int l = 0; l < st->n_layers; ++l)
-      if (st->layers[l].mlp != LR_MLP_SWIGLU) {
-        set_error("stack: the persistent step runs SiLU-GLU blocks only");
-        return LR_ERR_UNSUPPORTED;
-      }
+  if (st->mode != LR_STACK_AUTO && st->mode != LR_STACK_LAYERED) return invalid("stack: bad mode");
   if (!st->pool_in || !st->pool_out || !st->remap || !st->n_active || !st->xbuf || !st->h ||
       !st->ybuf || !st->scratch)
     return invalid("stack: null pointer");
@@ -659,10 +436,10 @@ lr_status enqueue_layered(const lr_stack_desc* st, cudaStream_t s) {
     if (r == LR_OK) r = launch_widen(st->xbuf, st->h, st->cap * d, s);
   }
   if (r != LR_OK) return r;
-  for (int l = 0; l < st->n_layers; ++l) {
-    r = enqueue_block(st->h, st->cap, &st->layers[l], ws, st->dev_status, s);
-    if (r != LR_OK) return r;
-  }
+  std::vector<Step> steps;
+  for (int l = 0; l < st->n_layers; ++l) block_steps(st->h, st->cap, &st->layers[l], ws, steps);
+  r = enqueue_steps(steps, st->cap, st->dev_status, s);
+  if (r != LR_OK) return r;
   if (decode)
     return launch_scatter_rows(st->h, st->ybuf, st->remap, st->n_active, st->pool_out,
                                st->pool_rows, d, st->cap, st->dev_status, s);
@@ -670,21 +447,6 @@ lr_status enqueue_layered(const lr_stack_desc* st, cudaStream_t s) {
   if (r != LR_OK) return r;
   return launch_scatter(st->ybuf, st->remap, st->n_active, st->pool_out, st->pool_rows,
                         row_bytes, st->cap, st->dev_status, s);
-}
-
-// Prepares (program upload, synchronous) and enqueues the persistent step.
-lr_status prepare_persist(const lr_stack_desc* st, cudaStream_t s, PersistParams* p, int* nt,
-                          void** zero_base, size_t* zero_bytes) {
-  lr_status r = ensure_configured();
-  if (r != LR_OK) return r;
-  Plan P;
-  build_plan(st, P);
-  r = upload_plan(st, P, s, p);
-  if (r != LR_OK) return r;
-  *nt = P.nt;
-  *zero_base = static_cast<uint8_t*>(st->scratch) + block_region_bytes(st) + P.off_zero;
-  *zero_bytes = P.zero_bytes;
-  return LR_OK;
 }
 
 }  // namespace
@@ -736,6 +498,29 @@ lr_status lr_linear_forward(const void* x, int64_t ldx, void* y, int64_t ldy, lr
   if (ws_bytes < lr_linear_workspace_bytes(M, f)) return invalid("linear: workspace too small");
   return enqueue_linear(x, ldx, y, ldy, y_dtype, M, f, workspace, dev_status,
                         reinterpret_cast<cudaStream_t>(s));
+}
+
+lr_status lr_factor_pack(const void* A, const void* B, int32_t d_in, int32_t d_out, int32_t r, void* At,
+                         void* Bt, lr_stream s) {
+  if (d_in <= 0 || d_out <= 0 || r <= 0) return invalid("factor_pack: non-positive dims");
+  if (d_in % 64 || d_out % 64 || r % 64) {
+    set_error("factor_pack: d_in=%d d_out=%d r=%d must be multiples of 64", d_in, d_out, r);
+    return LR_ERR_UNSUPPORTED;
+  }
+  if (!A || !B || !At || !Bt) return invalid("factor_pack: null pointer");
+  if (!aligned16(A) || !aligned16(B) || !aligned16(At) || !aligned16(Bt))
+    return invalid("factor_pack: pointers must be 16-byte aligned");
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(A), b0 = reinterpret_cast<uintptr_t>(B);
+  const uintptr_t at0 = reinterpret_cast<uintptr_t>(At), bt0 = reinterpret_cast<uintptr_t>(Bt);
+  const uintptr_t na = static_cast<uintptr_t>(d_in) * r * 2, nb = static_cast<uintptr_t>(r) * d_out * 2;
+  auto overlap = [](uintptr_t x, uintptr_t nx, uintptr_t y, uintptr_t ny) { return x < y + ny && y < x + nx; };
+  if (overlap(a0, na, at0, na) || overlap(a0, na, bt0, nb) || overlap(b0, nb, at0, na) ||
+      overlap(b0, nb, bt0, nb) || overlap(at0, na, bt0, nb))
+    return invalid("factor_pack: inputs and outputs must not overlap");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+  lr_status st = launch_transpose_bf16(A, d_in, r, At, cs);
+  if (st != LR_OK) return st;
+  return launch_transpose_bf16(B, r, d_out, Bt, cs);
 }
 
 size_t lr_block_scratch_bytes(int64_t M, const lr_block_desc* b) {
@@ -946,36 +731,19 @@ lr_status remap_build(const int32_t* lengths, int64_t n_seq, const int32_t* bloc
 
 size_t lr_stack_scratch_bytes(const lr_stack_desc* st) {
   if (st == nullptr || st->layers == nullptr || st->n_layers <= 0 || st->cap <= 0) return 0;
-  size_t n = block_region_bytes(st);
-  if (use_persist(st)) {
-    Plan P;
-    build_plan(st, P);
-    n += P.total;
-  }
-  return n;
+  return block_region_bytes(st);
 }
 
 lr_status lr_stack_forward(const lr_stack_desc* st, lr_stream s) {
   lr_status r = check_stack(st);
   if (r != LR_OK) return r;
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
-  if (!use_persist(st)) {
-    r = ensure_configured();
-    if (r != LR_OK) return r;
-    return enqueue_layered(st, cs);
-  }
-  PersistParams p;
-  int nt = 0;
-  void* zb = nullptr;
-  size_t zn = 0;
-  r = prepare_persist(st, cs, &p, &nt, &zb, &zn);
+  r = ensure_configured();
   if (r != LR_OK) return r;
-  return launch_persist(p, nt, zb, zn, cs);
+  return enqueue_layered(st, reinterpret_cast<cudaStream_t>(s));
 }
 
 int64_t lr_stack_launch_count(const lr_stack_desc* st) {
   if (st == nullptr || st->layers == nullptr) return 0;
-  if (use_persist(st)) return 1;
   const bool decode = st->cap <= kDecodeMaxRows;
   int64_t n = decode ? 2 : 4;  // gather(+widen), (narrow+)scatter
   for (int l = 0; l < st->n_layers; ++l) n += block_launches(st->cap, &st->layers[l]);
@@ -992,26 +760,18 @@ lr_status lr_graph_capture(const lr_stack_desc* st, lr_graph** out) {
   cudaStream_t cs = nullptr;
   cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
   if (e != cudaSuccess) return cuda_fail(e, "graph_capture: stream");
-  PersistParams p;
-  int nt = 0;
-  void* zb = nullptr;
-  size_t zn = 0;
-  const bool persist = use_persist(st);
-  if (persist) r = prepare_persist(st, cs, &p, &nt, &zb, &zn);
   lr_graph* g = new lr_graph();
-  if (r == LR_OK) {
-    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
-    if (e != cudaSuccess) {
-      r = cuda_fail(e, "graph_capture: begin");
-    } else {
-      lr_status r2 = persist ? launch_persist(p, nt, zb, zn, cs) : enqueue_layered(st, cs);
-      e = cudaStreamEndCapture(cs, &g->graph);
-      if (r2 != LR_OK) r = r2;
-      else if (e != cudaSuccess) r = cuda_fail(e, "graph_capture: end");
-      else {
-        e = cudaGraphInstantiate(&g->exec, g->graph, 0);
-        if (e != cudaSuccess) r = cuda_fail(e, "graph_capture: instantiate");
-      }
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) {
+    r = cuda_fail(e, "graph_capture: begin");
+  } else {
+    lr_status r2 = enqueue_layered(st, cs);
+    e = cudaStreamEndCapture(cs, &g->graph);
+    if (r2 != LR_OK) r = r2;
+    else if (e != cudaSuccess) r = cuda_fail(e, "graph_capture: end");
+    else {
+      e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+      if (e != cudaSuccess) r = cuda_fail(e, "graph_capture: instantiate");
     }
   }
   cudaStreamDestroy(cs);

@@ -333,4 +333,23 @@ lr_status launch_narrow(const float* in, void* out_bf16, int64_t n, cudaStream_t
                 reinterpret_cast<const float4*>(in), static_cast<uint4*>(out_bf16), n8);
 }
 
+// out[c][r] = in[r][c] for a bf16 [rows][cols] matrix (both multiples of 64):
+// one 64 x 64 tile per CTA through shared memory, bit-exact.
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __restrict__ in, int rows,
+                                                              int cols, uint16_t* __restrict__ out) {
+  __shared__ uint16_t tile[64][66];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
+  for (int i = ty; i < 64; i += 4) tile[i][tx] = in[static_cast<int64_t>(r0 + i) * cols + c0 + tx];
+  __syncthreads();
+  for (int i = ty; i < 64; i += 4) out[static_cast<int64_t>(c0 + i) * rows + r0 + tx] = tile[tx][i];
+}
+
+lr_status launch_transpose_bf16(const void* in, int rows, int cols, void* out, cudaStream_t s) {
+  return launch(transpose_bf16_kernel, dim3(cols / 64, rows / 64), dim3(256), s, "transpose",
+                static_cast<const uint16_t*>(in), rows, cols, static_cast<uint16_t*>(out));
+}
+
 }  // namespace lr

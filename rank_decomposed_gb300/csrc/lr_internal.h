@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+
 #include "../../include/lr.h"
 
 namespace lr {
@@ -89,64 +90,6 @@ struct PrefillParams {
   int32_t* status;
 };
 
-// ----------------------------------------------- persistent decode step
-// A decode step (compact -> L blocks -> scatter) as one cooperative kernel
-// that walks a program of phases separated by grid barriers.
-enum PhaseKind : int32_t {
-  PH_GEMM = 0,     // problems of a GEMM phase, split into segments (lr_persist.cu)
-  PH_GATHER = 1,   // h[i] = widen(pool[remap[i]]), xbuf[i] = pool[remap[i]]
-  PH_RMSNORM = 2,  // dst0 = bf16(rmsnorm(src0 fp32))
-  PH_SILU = 3,     // dst0 = bf16(silu(src0) * src1)
-  PH_SCATTER = 4,  // ybuf[i] = bf16(h[i]); pool_out[remap[i]] = ybuf[i]
-};
-
-struct PPhase {
-  int32_t kind;
-  int32_t d;            // row width (elements)
-  const void* src0;
-  const void* src1;
-  void* dst0;
-  void* dst1;
-  float eps;
-  int32_t pad_;
-};
-
-struct PProblem {
-  int32_t wmap, amap;   // tensor-map indices
-  int32_t N, nkb;
-  int32_t epi, vec_ok;
-  int32_t gqa_head_dim, gqa_group;
-  void* out;
-  int64_t ldo;
-};
-
-struct PSeg {           // kb range [kb0, kb1) of one 128-row tile
-  int32_t phase, prob, tile, kb0, kb1;
-  int32_t j, nc;        // contributor index / count of the tile (nc == 1: whole tile)
-  int32_t slot;         // first partial slot of the tile (nc > 1)
-  int32_t ctr;          // arrival counter of the tile (nc > 1)
-};
-
-struct PersistParams {
-  int32_t M;            // rows (= cap)
-  int32_t G;            // grid size
-  int32_t n_phases;
-  int32_t pf_ahead;     // weight tiles prefetched into L2 ahead of the smem ring
-  const PPhase* phases;
-  const PProblem* probs;
-  const PSeg* segs;
-  const int32_t* seg_begin;   // [G + 1]
-  const CUtensorMap* maps;
-  float* partials;            // slots of [NT][128] fp32
-  uint32_t* counters;
-  uint32_t* gbar;             // grid barrier arrivals
-  int32_t* abort_flag;
-  int32_t* status;
-  const int32_t* remap;
-  const int32_t* n_active;
-  int64_t pool_rows;
-};
-
 // ------------------------------------------------------------- host helpers
 void set_error(const char* fmt, ...);
 lr_status cuda_fail(cudaError_t e, const char* what);
@@ -186,6 +129,8 @@ lr_status launch_rmsnorm(const float* h, void* out_bf16, int64_t M, int d, float
 lr_status launch_silu_mul(const void* g, const void* u, void* out, int64_t M, int d,
                           cudaStream_t s);
 lr_status launch_widen(const void* in_bf16, float* out, int64_t n, cudaStream_t s);
+// out = in^T for bf16 [rows][cols], rows and cols multiples of 64.
+lr_status launch_transpose_bf16(const void* in, int rows, int cols, void* out, cudaStream_t s);
 lr_status launch_narrow(const float* in, void* out_bf16, int64_t n, cudaStream_t s);
 // Stack glue, one CTA per row: gather + widen, and narrow + scatter.
 lr_status launch_gather_rows(const void* pool, int64_t pool_rows, int d, const int32_t* remap,
@@ -205,13 +150,13 @@ lr_status launch_scatter(const void* buf, const int32_t* remap, const int32_t* n
 // device; done once per device before the first launch or capture.
 lr_status configure_decode();
 lr_status configure_prefill();
-lr_status configure_persist();
-// Enqueue the persistent step kernel (after a memset of counters/barrier).
-lr_status launch_persist(const PersistParams& p, int nt, void* zero_base, size_t zero_bytes,
-                         cudaStream_t s);
-int persist_max_rows();
-int persist_grid();
 lr_status ensure_configured();
+
+// Buffers of one block inside its scratch (offsets in bytes, 256-aligned).
+struct BlockLayout {
+  size_t n1, t[7], q, k, v, n2, g, u, a, total;
+};
+BlockLayout block_layout(int64_t M, const lr_block_desc* b);
 
 // Launch attribute helper: programmatic dependent launch on/off for kernels
 // enqueued by this library (on by default).

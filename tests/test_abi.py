@@ -198,3 +198,19 @@ def test_rank_sharded_argument_checks_launch_nothing():
     assert call(4, 5) == lr.LR_ERR_INVALID_ARG           # more shards than rank blocks
     assert call(4, 2, ws_bytes=100) == lr.LR_ERR_INVALID_ARG
     assert call(4, 2, y=0) == lr.LR_ERR_INVALID_ARG
+
+
+def test_factor_pack_argument_checks_launch_nothing():
+    """lr_factor_pack: every rejected call returns before any launch (no GPU here)."""
+    pack = lambda A, B, d_in, d_out, r, At, Bt: lr.lib.lr_factor_pack(A, B, d_in, d_out, r, At, Bt, None)
+    base = 0x100000
+    A, B = base, base + 0x100000
+    At, Bt = base + 0x200000, base + 0x300000
+    assert pack(A, B, 0, 64, 64, At, Bt) == lr.LR_ERR_INVALID_ARG
+    assert pack(A, B, 100, 64, 64, At, Bt) == lr.LR_ERR_UNSUPPORTED      # not a multiple of 64
+    assert pack(0, B, 64, 64, 64, At, Bt) == lr.LR_ERR_INVALID_ARG
+    assert pack(A + 2, B, 64, 64, 64, At, Bt) == lr.LR_ERR_INVALID_ARG    # misaligned
+    # A [64][64] bf16 = 8 KB: an At starting 4 KB into A overlaps it
+    assert pack(A, B, 64, 64, 64, A + 4096, Bt) == lr.LR_ERR_INVALID_ARG
+    assert pack(A, B, 64, 64, 64, At, At + 4096) == lr.LR_ERR_INVALID_ARG  # At and Bt overlap
+    assert "overlap" in lr.last_error()

@@ -115,10 +115,9 @@ def _oracle_stack(cfg, hosts, pool_bits, remap, n):
     return oracle.stack_forward(x, hosts, cfg["n_heads"], cfg["n_kv"], cfg["hd"])
 
 
-@pytest.mark.parametrize("mode", [lr.STACK_AUTO, lr.STACK_PERSISTENT])
-def test_stack_eager_graph_and_remap(mode):
+def test_stack_eager_graph_and_remap():
     cfg, cap = SMALL, 16
-    stack, hosts, pool_bits, remap, n = _make_stack(cfg, 3, cap, 12, mode=mode)
+    stack, hosts, pool_bits, remap, n = _make_stack(cfg, 3, cap, 12)
     assert n == 12
     stack.forward()
     torch.cuda.synchronize()
@@ -172,44 +171,36 @@ def test_stack_launch_count():
     # gather + widen, 2 RMSNorm + 8 GEMM + SiLU-GLU launches per block, narrow + scatter
     stack, *_ = _make_stack(SMALL, 2, 8, 6, mode=lr.STACK_LAYERED)
     assert stack.launch_count() == 2 + 2 * 11
-    stack, *_ = _make_stack(SMALL, 2, 8, 6, mode=lr.STACK_PERSISTENT)
-    assert stack.launch_count() == 1
 
 
 @pytest.mark.parametrize("cap,n_seq", [(1, 1), (16, 16), (100, 90), (256, 256)])
-def test_persistent_stack_caps(cap, n_seq):
-    """Every token tile width of the persistent kernel (16, 32->64, 128, 256) against the oracle."""
+def test_stack_caps(cap, n_seq):
+    """Every token tile width of the decode kernel (16, 32->64, 128, 256) in a graph step."""
     cfg = SMALL
-    stack, hosts, pool_bits, remap, n = _make_stack(cfg, 2, cap, n_seq, seed=5,
-                                                    mode=lr.STACK_PERSISTENT)
+    stack, hosts, pool_bits, remap, n = _make_stack(cfg, 2, cap, n_seq, seed=5)
     stack.capture()
     stack.replay()
     torch.cuda.synchronize()
     assert int(stack.status.item()) == 0
     ref = _oracle_stack(cfg, hosts, pool_bits, remap, n)
-    assert_parity(stack.h[:n].cpu().numpy(), ref, "persistent cap=%d" % cap)
+    assert_parity(stack.h[:n].cpu().numpy(), ref, "stack cap=%d" % cap)
     stack.destroy()
 
 
-def test_persistent_matches_layered_llama7b():
-    """Two 7B-shaped layers, 64 rows: persistent and layered steps against the oracle and each other."""
+def test_stack_llama7b_two_layers():
+    """Two 7B-shaped layers, 64 rows, replayed twice: the layers' contribution against the oracle."""
     cfg, cap = LLAMA7B, 64
-    outs = []
-    for mode in (lr.STACK_PERSISTENT, lr.STACK_LAYERED):
-        stack, hosts, pool_bits, remap, n = _make_stack(cfg, 2, cap, 64, seed=6, mode=mode)
-        stack.capture()
-        for _ in range(2):
-            stack.replay()
-        torch.cuda.synchronize()
-        assert int(stack.status.item()) == 0
-        outs.append(stack.h.clone())
-        stack.destroy()
+    stack, hosts, pool_bits, remap, n = _make_stack(cfg, 2, cap, 64, seed=6)
+    stack.capture()
+    for _ in range(2):
+        stack.replay()
+    torch.cuda.synchronize()
+    assert int(stack.status.item()) == 0
     ref = _oracle_stack(cfg, hosts, pool_bits, remap, n)
     x0 = oracle.widen_bf16(pool_bits[remap[:n]])
-    for h in outs:
-        out = h[:n].cpu().numpy().astype(np.float64)
-        assert_parity(out - x0, ref - x0, "7B stack delta")
-    assert_parity(outs[0].cpu().numpy(), outs[1].cpu().numpy(), "persistent vs layered")
+    out = stack.h[:n].cpu().numpy().astype(np.float64)
+    assert_parity(out - x0, ref - x0, "7B stack delta")
+    stack.destroy()
 
 
 OPT_SMALL = dict(d=512, d_ff=2048, n_heads=8, n_kv=8, hd=64, ranks=(128, 128, 128, 128, 64, 192, 192),
@@ -259,6 +250,53 @@ def test_stack_with_per_layer_ranks():
     assert int(stack.status.item()) == 0
     ref = _oracle_stack(SMALL, list(hosts), pool_bits, remap, n)
     assert_parity(stack.h[:n].cpu().numpy(), ref, "variadic-rank stack")
+    stack.destroy()
+
+
+@pytest.mark.parametrize("cfg_name,cap", [("opt", 16), ("opt", 64), ("mqa", 37), ("mqa", 128)])
+def test_stack_variants(cfg_name, cap):
+    """Graph steps of a non-GLU (ReLU) MLP stack and an MQA stack."""
+    cfg = OPT_SMALL if cfg_name == "opt" else MQA_SMALL
+    stack, hosts, pool_bits, remap, n = _make_stack(cfg, 3, cap, cap, seed=16)
+    stack.capture()
+    stack.replay()
+    torch.cuda.synchronize()
+    assert int(stack.status.item()) == 0
+    x = oracle.widen_bf16(pool_bits[remap[:n]])
+    ref = oracle.stack_forward(x, hosts, cfg["n_heads"], cfg["n_kv"], cfg["hd"], mlp=cfg.get("mlp", "swiglu"))
+    out = stack.h[:n].cpu().numpy().astype(np.float64)
+    assert_parity(out - x, ref - x, "stack %s cap=%d" % (cfg_name, cap))
+    stack.destroy()
+
+
+def test_per_layer_ranks_and_replay_determinism():
+    """Layers at different ranks in one graph step (48 rows); two replays agree bit for bit."""
+    cfgs = (SMALL, dict(SMALL, ranks=(64, 64, 64, 64, 64, 64, 64)),
+            dict(SMALL, ranks=(256, 128, 128, 256, 320, 320, 320)))
+    layers, hosts = zip(*[make_layer(17, l, c) for l, c in enumerate(cfgs)])
+    cap, d = 48, SMALL["d"]
+    L, table, total = synth.paged_batch(17, 40, 20, 300, 16)
+    pool_bits = synth.bf16_normal(17, synth.make_tag(0, 0, synth.KIND_POOL), (total * 16, d))
+    remap, n, _ = lr.remap_build(L, table, 16, 1, cap)
+    pool = dev_bits(pool_bits)
+    stack = lr.Stack(list(layers), pool, pool.clone(), torch.from_numpy(remap).cuda(),
+                     torch.tensor([n], dtype=torch.int32, device="cuda"),
+                     torch.zeros(cap, d, dtype=torch.bfloat16, device="cuda"),
+                     torch.zeros(cap, d, dtype=torch.float32, device="cuda"),
+                     torch.zeros(cap, d, dtype=torch.bfloat16, device="cuda"),
+                     torch.zeros(lr.Stack.scratch_bytes(cap, layers), dtype=torch.uint8, device="cuda"),
+                     torch.zeros(1, dtype=torch.int32, device="cuda"))
+    stack.capture()
+    stack.replay()
+    torch.cuda.synchronize()
+    h1 = stack.h.clone()
+    stack.h.fill_(7.0)
+    stack.replay()
+    torch.cuda.synchronize()
+    assert int(stack.status.item()) == 0
+    assert torch.equal(stack.h, h1)
+    ref = _oracle_stack(SMALL, list(hosts), pool_bits, remap, n)
+    assert_parity(stack.h[:n].cpu().numpy(), ref, "variadic-rank stack, 48 rows")
     stack.destroy()
 
 

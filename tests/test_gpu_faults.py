@@ -47,3 +47,4 @@ def test_bounded_wait_reports_timeout_and_gpu_recovers(shape):
     A, B = host_factor(21, 0, 0, d_in, d_out, r)
     assert_parity(y.cpu().numpy(), oracle.lowrank_linear(oracle.widen_bf16(x_bits), A, B)[1],
                   "after timeout")
+

@@ -66,7 +66,17 @@ def test_noalloc_equals_workspace_entry_point_twice(M, shape, ydtype, ld_extra):
         if ld_extra:                                  # the padding columns are not written
             assert torch.isnan(y_full[:, d_out:].float()).all()
         want = oracle.lowrank_linear(oracle.widen_bf16(x_bits), A, B)[1]
-        assert_parity(y.float().cpu().numpy(), want, "noalloc call %d vs oracle" % call)
+        if ydtype == torch.float32:
+            assert_parity(y.cpu().numpy(), want, "noalloc call %d vs oracle" % call)
+        else:
+            # a bf16 y is the round-to-nearest-even image of the fp32 y, whose
+            # parity is what the oracle checks (bf16 rounding alone can exceed
+            # the bar at this rms)
+            y32 = torch.empty((M, d_out), dtype=torch.float32, device="cuda")
+            assert _call_noalloc(x, f, y32, st) == lr.LR_OK, lr.last_error()
+            torch.cuda.synchronize()
+            assert torch.equal(y, y32.to(torch.bfloat16))
+            assert_parity(y32.cpu().numpy(), want, "noalloc call %d (fp32) vs oracle" % call)
 
 
 def test_noalloc_python_wrapper():
