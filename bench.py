@@ -420,48 +420,81 @@ def time_prefill(torch, lr, M=16384, rhos=(0.2, 0.4, 0.6), reps=3, m=LLAMA7B):
     return out
 
 
-def time_kv_reconstruct(torch, lr, m=LLAMA7B, n_seq=64, reps=5):
+def time_kv_reconstruct(torch, lr, m=LLAMA7B, n_seq=64, reps=5, hbm=None, tf=None):
     """Low-rank KV reconstruction of a whole decode batch's context.
 
-    Every position of 64 sequences (lengths U{128..4096}) is listed by
-    remap_build, its k latent (r columns) compacted into a fixed buffer, and
-    multiplied by B_k in one fixed-size GEMM, as the pages' graph-replay stage.
+    Every position of 64 sequences (lengths U{128..4096}) is rebuilt from its
+    k latent (r columns) by one fixed-size GEMM with B_k, as in the pages'
+    graph-replay stage, two ways: row-level (remap_build lists every position,
+    remap_compact copies the latents into a [cap, r] buffer, then the GEMM),
+    and block-level (remap_build_blocks lists the paged blocks and the GEMM
+    reads them straight from the pool: one launch, no buffer).  Reported for
+    the model's k projection and for the LLaMA-70B-GQA k shape (576 -> 1024).
     """
-    d_kv = m.nkv * m.hd
-    r = rank_for(m.d, d_kv, RHO)
+    shapes_kv = [("%s_k" % m.name, rank_for(m.d, m.nkv * m.hd, RHO), m.nkv * m.hd)]
+    if m.name != "llama70b":
+        shapes_kv.append(("llama70b_k", rank_for(LLAMA70B.d, LLAMA70B.nkv * LLAMA70B.hd, RHO),
+                          LLAMA70B.nkv * LLAMA70B.hd))
     L, table, pool_rows = batch(7, n_seq, n_seq)
     cap = int(L.sum())
     remap, n, runs = lr.remap_build(L, table, BLOCK_ROWS, 0, cap)
-    pool = torch.empty((pool_rows, r), dtype=torch.bfloat16, device="cuda")
-    synth.fill_bf16_normal_device(pool.data_ptr(), pool_rows, r, 7, synth.make_tag(0, 1, synth.KIND_POOL), 1.0)
-    _, sg = synth.factor_stds(m.d, r)
-    Bt = torch.empty((d_kv, r), dtype=torch.bfloat16, device="cuda")
-    cs = torch.from_numpy(synth.sigma_scale(r)).cuda()
-    synth.fill_bf16_normal_device(Bt.data_ptr(), d_kv, r, 7, synth.make_tag(0, synth.PROJ_K, synth.KIND_B), sg,
-                                  cs.data_ptr())
-    buf = torch.empty((cap, r), dtype=torch.bfloat16, device="cuda")
-    out = torch.empty((cap, d_kv), dtype=torch.bfloat16, device="cuda")
-    d_remap = torch.from_numpy(remap).cuda()
-    d_n = torch.tensor([n], dtype=torch.int32, device="cuda")
-    st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    lr.kv_reconstruct(pool, d_remap, d_n, buf, Bt, out, st)
-    torch.cuda.synchronize()
-    best = None
-    for _ in range(reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        lr.kv_reconstruct(pool, d_remap, d_n, buf, Bt, out, st)
-        e1.record()
+    cap_b = int(sum((int(x) + BLOCK_ROWS - 1) // BLOCK_ROWS for x in L))
+    blocks, nb, bruns = lr.remap_build_blocks(L, table, BLOCK_ROWS, cap_b)
+    res = {"rows": cap, "blocks": nb, "remap_runs": runs, "block_runs": bruns, "shapes": []}
+
+    def best_of(fn):
+        fn()
         torch.cuda.synchronize()
-        t = e0.elapsed_time(e1) * 1e-3
-        best = t if best is None else min(best, t)
-    if int(st.item()) != 0:
-        raise SystemExit("kv_reconstruct status %d" % int(st.item()))
-    flops = 2.0 * cap * r * d_kv
-    nbytes = 2.0 * cap * r * 2 + 2.0 * cap * d_kv + 2.0 * d_kv * r   # gather r/w, out, Bt
-    return {"rows": cap, "r": r, "d_kv": d_kv, "remap_runs": runs, "ms": round(best * 1e3, 4),
-            "rows_per_s": round(cap / best, 1), "tflops": round(flops / best / 1e12, 1),
-            "gbs": round(nbytes / best / 1e9, 1)}
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) * 1e-3
+            best = t if best is None else min(best, t)
+        return best
+
+    for name, r, d_kv in shapes_kv:
+        pool = torch.empty((pool_rows, r), dtype=torch.bfloat16, device="cuda")
+        synth.fill_bf16_normal_device(pool.data_ptr(), pool_rows, r, 7, synth.make_tag(0, 1, synth.KIND_POOL), 1.0)
+        _, sg = synth.factor_stds(m.d, r)
+        Bt = torch.empty((d_kv, r), dtype=torch.bfloat16, device="cuda")
+        cs = torch.from_numpy(synth.sigma_scale(r)).cuda()
+        synth.fill_bf16_normal_device(Bt.data_ptr(), d_kv, r, 7, synth.make_tag(0, synth.PROJ_K, synth.KIND_B), sg,
+                                      cs.data_ptr())
+        buf = torch.empty((cap, r), dtype=torch.bfloat16, device="cuda")
+        out = torch.empty((cap, d_kv), dtype=torch.bfloat16, device="cuda")
+        out_b = torch.empty((cap_b * BLOCK_ROWS, d_kv), dtype=torch.bfloat16, device="cuda")
+        d_remap = torch.from_numpy(remap).cuda()
+        d_n = torch.tensor([n], dtype=torch.int32, device="cuda")
+        d_blocks = torch.from_numpy(blocks).cuda()
+        d_nb = torch.tensor([nb], dtype=torch.int32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        t_row = best_of(lambda: lr.kv_reconstruct(pool, d_remap, d_n, buf, Bt, out, st))
+        t_blk = best_of(lambda: lr.kv_reconstruct_paged(pool, d_blocks, d_nb, Bt, out_b, st))
+        if int(st.item()) != 0:
+            raise SystemExit("kv_reconstruct status %d" % int(st.item()))
+        rows_b = cap_b * BLOCK_ROWS
+        flops = 2.0 * rows_b * r * d_kv
+        # algorithmic bytes: the latent rows read once, B_k, the reconstructed rows written
+        nbytes_b = 2.0 * rows_b * r + 2.0 * d_kv * r + 2.0 * rows_b * d_kv
+        nbytes_r = 2.0 * cap * r * 2 + 2.0 * d_kv * r + 2.0 * cap * d_kv     # + the buffer written and read
+        entry = {"shape": name, "r": r, "d_kv": d_kv,
+                 "row_level": {"ms": round(t_row * 1e3, 4), "rows_per_s": round(cap / t_row, 1),
+                               "gbs": round(nbytes_r / t_row / 1e9, 1)},
+                 "paged": {"ms": round(t_blk * 1e3, 4), "rows_per_s": round(cap / t_blk, 1),
+                           "gbs": round(nbytes_b / t_blk / 1e9, 1), "tflops": round(flops / t_blk / 1e12, 1),
+                           "algorithmic_bytes": nbytes_b, "rows_computed": rows_b}}
+        if hbm:
+            entry["paged"]["frac_of_hbm"] = round(nbytes_b / t_blk / 1e9 / hbm, 4)
+        if tf:
+            entry["paged"]["frac_of_bf16_peak"] = round(flops / t_blk / 1e12 / tf, 4)
+        res["shapes"].append(entry)
+        del pool, Bt, buf, out, out_b
+        torch.cuda.empty_cache()
+    return res
 
 
 def rank_sharding(torch, lr, M=64, Gs=(2, 4, 8), rho=RHO, m=None, reps=20):
@@ -673,7 +706,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the M sweep, eager and prefill legs")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
     ap.add_argument("--no-config4", action="store_true", help="skip the LLaMA-70B-shaped legs")
-    ap.add_argument("--only", choices=["roofline", "prefill"],
+    ap.add_argument("--only", choices=["roofline", "prefill", "kv"],
                     help="run one leg alone (for profiling): the event-timed decode linears, or "
                          "the prefill projections at rho=0.4")
     args = ap.parse_args()
@@ -710,6 +743,11 @@ def main():
         torch.cuda.set_device(0)
     barrier = (lambda: dist.barrier()) if dist else None
 
+    if args.only == "kv":
+        hbm, tf, _ = load_peaks()
+        print(json.dumps({"leg": "kv_reconstruct", "config": model.name,
+                          "result": time_kv_reconstruct(torch, lr, m=model, hbm=hbm, tf=tf)}))
+        return
     if args.only == "prefill":
         M = 8 * 4096 if model.name == "llama70b" else 16384
         print(json.dumps({"leg": "prefill", "config": model.name, "M": M,
@@ -807,7 +845,7 @@ def main():
             line["prefill"] = prefill_summary(time_prefill(torch, lr, M=pm, m=model,
                                                            rhos=(0.2, 0.4, 0.6) if model.name == "llama7b" else (0.4,)),
                                               model, pm, tf)
-            line["kv_reconstruct"] = time_kv_reconstruct(torch, lr, m=model)
+            line["kv_reconstruct"] = time_kv_reconstruct(torch, lr, m=model, hbm=hbm, tf=tf)
             line["rank_sharding"] = rank_sharding(torch, lr)
             if model.name == "llama7b" and not args.no_config4:
                 line["config4"] = config4(torch, lr, tf, max(10, args.steps // 2))

@@ -237,6 +237,59 @@ lr_status lr_kv_reconstruct(const void* latent_pool, int64_t pool_rows, int32_t 
                             int32_t* dev_status, lr_stream s);
 
 /* ---------------------------------------------------------------------------
+ * The block-granular form of the same reconstruction: the remap lists whole
+ * paged blocks (the pages' "new block table", English page section 2.C), and
+ * the up-projection GEMM reads each listed block straight from the latent
+ * pool -- no compacted copy is written or read back.
+ *
+ * remap_build_blocks (host only): for each sequence in order, the physical
+ * blocks that hold its positions 0 .. L-1 (the first ceil(L / block_rows)
+ * entries of its block-table row).
+ *   lengths: host int32 [n_seq]; block_table: host int32 [n_seq][blocks_per_seq].
+ *   Outputs (host): blocks_out[cap_blocks] (unused entries -1), *n_blocks_out,
+ *   *n_runs_out = maximal runs of consecutive block ids.
+ *   LR_ERR_INVALID_ARG if the blocks exceed cap_blocks, a needed entry is
+ *   negative, a length does not fit its table row, or a block is listed twice.
+ *   Position p of sequence s sits at row block_rows * i + p % block_rows of
+ *   the reconstruction, i being the list index of its block. */
+lr_status remap_build_blocks(const int32_t* lengths, int64_t n_seq, const int32_t* block_table,
+                             int32_t blocks_per_seq, int32_t block_rows, int64_t cap_blocks,
+                             int32_t* blocks_out, int32_t* n_blocks_out, int32_t* n_runs_out);
+
+/* lr_kv_latent_write: the producer side of the low-rank KV cache (English
+ * page section 1: the latent KV grows with the context; section 2.C: it is
+ * kept in paged memory).  The down projection of k or v for M new tokens is
+ * written straight into their rows of the paged latent pool:
+ *   latent_pool[rows[m]][:] = bf16(x[m] A_r)   for m < M,
+ * summed in fp32 and rounded to nearest even, with A_r given transposed as
+ * At [r][d_in].  x: device bf16 [M][ldx]; rows: device int32 [M] (for one new
+ * token per sequence, remap_build with tail_rows = 1 on the grown lengths);
+ * latent_pool: device bf16 [pool_rows][r].  d_in, r positive multiples of 64;
+ * pointers 16-byte aligned, ldx >= d_in and a multiple of 8.  Entries of rows
+ * outside [0, pool_rows) are skipped and reported as LR_ERR_REMAP_RANGE;
+ * rows must be distinct.  Other pool rows are not touched.  The values are
+ * those the down launch of lr_linear_forward writes for t.  M = 0 is a
+ * no-op. */
+lr_status lr_kv_latent_write(const void* x, int64_t ldx, int64_t M, const void* At, int32_t d_in, int32_t r,
+                             const int32_t* rows, void* latent_pool, int64_t pool_rows, int32_t* dev_status,
+                             lr_stream s);
+
+/* lr_kv_reconstruct_paged: with 16-row blocks,
+ *   out[16 i + j][n] = sum_c latent_pool[16 blocks[i] + j][c] * B_r[c][n]
+ * for i < *n_blocks and j < 16; rows of blocks i >= *n_blocks are zero.
+ *   latent_pool: device bf16 [pool_blocks * 16][r]; blocks: device int32
+ *   [cap_blocks]; n_blocks: device int32 (read on the device, so a captured
+ *   graph serves every batch); Bt: device bf16 [d_kv][r]; out: device bf16
+ *   [cap_blocks * 16][d_kv].  r and d_kv positive multiples of 64; pointers
+ *   16-byte aligned.  A listed block outside [0, pool_blocks) reads as zeros
+ *   and reports LR_ERR_REMAP_RANGE.  The rows past a sequence's length in its
+ *   last block are reconstructed from whatever the pool holds there; the
+ *   caller ignores them.  One launch. */
+lr_status lr_kv_reconstruct_paged(const void* latent_pool, int64_t pool_blocks, int32_t r, const int32_t* blocks,
+                                  const int32_t* n_blocks, int64_t cap_blocks, const void* Bt, int32_t d_kv,
+                                  void* out, int32_t* dev_status, lr_stream s);
+
+/* ---------------------------------------------------------------------------
  * Rank-space sharding of one factorized linear, simulated on this GPU (English
  * page section 2.A, "Highly Efficient Low-Rank Communication": the down
  * projection is split by columns and its output all-gathered in the low-rank

@@ -239,6 +239,74 @@ def kv_reconstruct(latent_pool: np.ndarray, remap, n_active: int, cap: int, B: n
     return buf, np.asarray(buf, dtype=np.float64) @ np.asarray(B, dtype=np.float64), bad
 
 
+def kv_latent_write(x, A, rows, pool):
+    """The latent KV producer (English page, sections 1 and 2.C).
+
+    Row m of the down projection x A (x [M, d_in], A [d_in, r]) is written to
+    row rows[m] of the paged latent pool [pool_rows, r]; other rows keep their
+    contents.  Entries outside the pool are skipped and set the returned flag.
+    fp64, no rounding; returns (pool', flag).
+    """
+    t = np.asarray(x, dtype=np.float64) @ np.asarray(A, dtype=np.float64)
+    out = np.array(pool, dtype=np.float64, copy=True)
+    bad = False
+    for m, j in enumerate(rows):
+        j = int(j)
+        if 0 <= j < out.shape[0]:
+            out[j] = t[m]
+        else:
+            bad = True
+    return out, bad
+
+
+def remap_build_blocks(lengths, block_table, block_rows: int, cap_blocks: int):
+    """Preparation stage at block granularity (English page, section 2.C: the
+    remapping index list as a new block table).
+
+    For each sequence in order, the physical blocks holding its positions
+    0 .. L-1: the first ceil(L / block_rows) entries of its block-table row.
+    Returns ``(blocks[cap_blocks], n_blocks, n_runs)`` with unused entries -1
+    and ``n_runs`` the maximal runs of consecutive block ids.  Raises
+    ValueError when the blocks exceed ``cap_blocks`` or an entry is missing.
+    """
+    out = []
+    for s, L in enumerate(lengths):
+        nb = (int(L) + block_rows - 1) // block_rows
+        for b in range(nb):
+            blk = int(block_table[s][b])
+            if blk < 0:
+                raise ValueError("block table entry missing")
+            out.append(blk)
+    if len(out) > cap_blocks:
+        raise ValueError("blocks exceed capacity")
+    blocks = np.full(cap_blocks, -1, dtype=np.int32)
+    blocks[: len(out)] = out
+    n_runs = sum(1 for i in range(len(out)) if i == 0 or out[i] != out[i - 1] + 1)
+    return blocks, len(out), n_runs
+
+
+def kv_reconstruct_paged(latent_pool: np.ndarray, blocks, n_blocks: int, B: np.ndarray, block_rows: int = 16):
+    """Reconstruction of whole listed blocks (English page, section 2.C).
+
+    Row ``block_rows * i + j`` of the result is row ``j`` of block
+    ``blocks[i]`` of the paged latent pool times the up factor B [r, d_kv], for
+    i < n_blocks; the rows of the other list entries are zero.  A block id
+    outside the pool gives zero rows and sets the returned flag.  fp64.
+    """
+    cap = len(blocks)
+    r = latent_pool.shape[1]
+    buf = np.zeros((cap * block_rows, r), dtype=np.float64)
+    bad = False
+    pool_blocks = latent_pool.shape[0] // block_rows
+    for i in range(min(n_blocks, cap)):
+        b = int(blocks[i])
+        if 0 <= b < pool_blocks:
+            buf[i * block_rows:(i + 1) * block_rows] = latent_pool[b * block_rows:(b + 1) * block_rows]
+        else:
+            bad = True
+    return buf @ np.asarray(B, dtype=np.float64), bad
+
+
 # ------------------------------------------------------ rank-space sharding
 def shard_columns(n: int, G: int):
     """Split n columns (a multiple of 64) over G processes in whole 64-column blocks.

@@ -84,6 +84,9 @@ def _load():
         "remap_scatter": (i32, [vp, vp, vp, vp, i64, i64, i64, vp, vp]),
         "remap_build": (i32, [vp, i64, vp, i32, i32, i32, i64, vp, vp, vp]),
         "lr_kv_reconstruct": (i32, [vp, i64, i32, vp, vp, i64, vp, vp, i32, vp, vp, vp]),
+        "remap_build_blocks": (i32, [vp, i64, vp, i32, i32, i64, vp, vp, vp]),
+        "lr_kv_latent_write": (i32, [vp, i64, i64, vp, i32, i32, vp, vp, i64, vp, vp]),
+        "lr_kv_reconstruct_paged": (i32, [vp, i64, i32, vp, vp, i64, vp, i32, vp, vp, vp]),
         "lr_rank_sharded_workspace_bytes": (sz, [i64, P(Factor), i32]),
         "lr_linear_forward_rank_sharded": (i32, [vp, i64, vp, i64, i32, i64, P(Factor), i32, vp, sz,
                                                  vp, vp]),
@@ -354,6 +357,49 @@ def kv_reconstruct(latent_pool, remap, n_active, latent_buf, Bt, out, status, st
                                Bt.data_ptr(), Bt.shape[0], out.data_ptr(), _ptr(status),
                                _stream(stream))
     _check("lr_kv_reconstruct", st)
+
+
+def remap_build_blocks(lengths, block_table, block_rows: int, cap_blocks: int):
+    """Host scan at block granularity: returns (blocks int32[cap_blocks], n_blocks, n_runs)."""
+    L = np.ascontiguousarray(lengths, dtype=np.int32)
+    T = np.ascontiguousarray(block_table, dtype=np.int32)
+    if T.ndim != 2 or T.shape[0] != L.shape[0]:
+        raise ValueError("block_table must be [n_seq][blocks_per_seq]")
+    out = np.empty(cap_blocks, dtype=np.int32)
+    nb = ctypes.c_int32(0)
+    nr = ctypes.c_int32(0)
+    st = lib.remap_build_blocks(L.ctypes.data, L.shape[0], T.ctypes.data, T.shape[1], block_rows, cap_blocks,
+                                out.ctypes.data, ctypes.byref(nb), ctypes.byref(nr))
+    _check("remap_build_blocks", st)
+    return out, nb.value, nr.value
+
+
+def kv_latent_write(x, At, rows, latent_pool, status, stream=None):
+    """latent_pool[rows[m]] = bf16(x[m] A_r) for the M rows of x (At = A_r^T [r][d_in])."""
+    _bf16(x, "x")
+    _bf16(At, "At")
+    _bf16(latent_pool, "latent_pool")
+    r, d_in = At.shape
+    if x.shape[1] != d_in or latent_pool.shape[1] != r or rows.shape[0] != x.shape[0]:
+        raise ValueError("kv_latent_write: inconsistent shapes")
+    st = lib.lr_kv_latent_write(x.data_ptr(), x.stride(0), x.shape[0], At.data_ptr(), d_in, r, rows.data_ptr(),
+                                latent_pool.data_ptr(), latent_pool.shape[0], _ptr(status), _stream(stream))
+    _check("lr_kv_latent_write", st)
+
+
+def kv_reconstruct_paged(latent_pool, blocks, n_blocks, Bt, out, status, stream=None):
+    """out[16 i + j] = latent_pool[16 blocks[i] + j] B_r for i < n_blocks (zero rows after)."""
+    _bf16(latent_pool, "latent_pool")
+    _bf16(Bt, "Bt")
+    _bf16(out, "out")
+    r = latent_pool.shape[1]
+    if latent_pool.shape[0] % 16 or Bt.shape[1] != r or out.shape[1] != Bt.shape[0] \
+            or out.shape[0] != 16 * blocks.shape[0]:
+        raise ValueError("kv_reconstruct_paged: inconsistent shapes")
+    st = lib.lr_kv_reconstruct_paged(latent_pool.data_ptr(), latent_pool.shape[0] // 16, r, blocks.data_ptr(),
+                                     n_blocks.data_ptr(), blocks.shape[0], Bt.data_ptr(), Bt.shape[0],
+                                     out.data_ptr(), _ptr(status), _stream(stream))
+    _check("lr_kv_reconstruct_paged", st)
 
 
 # ---------------------------------------------------------------- stack

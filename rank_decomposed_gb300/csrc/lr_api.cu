@@ -691,6 +691,82 @@ lr_status lr_rank_shard_comm_bytes(int64_t M, int32_t d_out, int32_t r, int32_t 
   return LR_OK;
 }
 
+lr_status remap_build_blocks(const int32_t* lengths, int64_t n_seq, const int32_t* block_table,
+                             int32_t blocks_per_seq, int32_t block_rows, int64_t cap_blocks,
+                             int32_t* blocks_out, int32_t* n_blocks_out, int32_t* n_runs_out) {
+  if (n_seq < 0 || cap_blocks < 0 || block_rows <= 0 || blocks_per_seq < 0)
+    return invalid("remap_build_blocks: bad sizes");
+  if ((n_seq > 0 && (!lengths || !block_table)) || (cap_blocks > 0 && !blocks_out) || !n_blocks_out ||
+      !n_runs_out)
+    return invalid("remap_build_blocks: null pointer");
+  int64_t n = 0;
+  for (int64_t s = 0; s < n_seq; ++s) {
+    const int64_t L = lengths[s];
+    if (L < 0 || L > static_cast<int64_t>(blocks_per_seq) * block_rows)
+      return invalid("remap_build_blocks: length %lld of sequence %lld does not fit its table row",
+                     (long long)L, (long long)s);
+    const int64_t nb = (L + block_rows - 1) / block_rows;
+    for (int64_t b = 0; b < nb; ++b) {
+      const int32_t blk = block_table[s * blocks_per_seq + b];
+      if (blk < 0) return invalid("remap_build_blocks: missing block for sequence %lld", (long long)s);
+      if (n >= cap_blocks) return invalid("remap_build_blocks: blocks exceed cap %lld", (long long)cap_blocks);
+      blocks_out[n++] = blk;
+    }
+  }
+  std::vector<int32_t> sorted(blocks_out, blocks_out + n);
+  std::sort(sorted.begin(), sorted.end());
+  if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
+    return invalid("remap_build_blocks: a physical block is listed twice");
+  int32_t runs = 0;
+  for (int64_t i = 0; i < n; ++i)
+    if (i == 0 || blocks_out[i] != blocks_out[i - 1] + 1) ++runs;
+  for (int64_t i = n; i < cap_blocks; ++i) blocks_out[i] = -1;
+  *n_blocks_out = static_cast<int32_t>(n);
+  *n_runs_out = runs;
+  return LR_OK;
+}
+
+lr_status lr_kv_latent_write(const void* x, int64_t ldx, int64_t M, const void* At, int32_t d_in, int32_t r,
+                             const int32_t* rows, void* latent_pool, int64_t pool_rows, int32_t* dev_status,
+                             lr_stream s) {
+  if (d_in <= 0 || r <= 0 || M < 0 || pool_rows < 0) return invalid("kv_latent_write: bad sizes");
+  if (d_in % 64 || r % 64) {
+    set_error("kv_latent_write: d_in=%d and r=%d must be multiples of 64", d_in, r);
+    return LR_ERR_UNSUPPORTED;
+  }
+  if (M == 0) return LR_OK;
+  if (M > 0x7FFFFFFF) return invalid("kv_latent_write: bad M");
+  if (!x || !At || !rows || !latent_pool) return invalid("kv_latent_write: null pointer");
+  if (ldx < d_in || ldx % 8 || !aligned16(x) || !aligned16(At) || !aligned16(latent_pool))
+    return invalid("kv_latent_write: x, At and the pool must be 16-byte aligned with ldx >= d_in, ldx %% 8 == 0");
+  GemmOp down = make_op(At, r, d_in, x, ldx, d_in, EPI_STORE_BF16, latent_pool, r);
+  down.out_rows = rows;
+  down.out_rows_limit = pool_rows;
+  return run_ops(M, &down, 1, dev_status, reinterpret_cast<cudaStream_t>(s));
+}
+
+lr_status lr_kv_reconstruct_paged(const void* latent_pool, int64_t pool_blocks, int32_t r, const int32_t* blocks,
+                                  const int32_t* n_blocks, int64_t cap_blocks, const void* Bt, int32_t d_kv,
+                                  void* out, int32_t* dev_status, lr_stream s) {
+  if (r <= 0 || d_kv <= 0 || cap_blocks < 0 || pool_blocks < 0)
+    return invalid("kv_reconstruct_paged: bad sizes");
+  if (r % 64 || d_kv % 64) {
+    set_error("kv_reconstruct_paged: r=%d and d_kv=%d must be multiples of 64", r, d_kv);
+    return LR_ERR_UNSUPPORTED;
+  }
+  if (cap_blocks == 0) return LR_OK;
+  if (pool_blocks * kPageRows > 0x7FFFFFFF || cap_blocks * kPageRows > 0x7FFFFFFF)
+    return invalid("kv_reconstruct_paged: pool or capacity rows overflow int32");
+  if (!latent_pool || !blocks || !n_blocks || !Bt || !out) return invalid("kv_reconstruct_paged: null pointer");
+  if (!aligned16(latent_pool) || !aligned16(Bt) || !aligned16(out))
+    return invalid("kv_reconstruct_paged: buffers must be 16-byte aligned");
+  lr_status st = ensure_configured();
+  if (st != LR_OK) return st;
+  GemmOp up = make_op(Bt, d_kv, r, latent_pool, r, r, EPI_STORE_BF16, out, d_kv);
+  return launch_prefill_paged(cap_blocks * kPageRows, up, blocks, n_blocks, pool_blocks, dev_status,
+                              reinterpret_cast<cudaStream_t>(s));
+}
+
 lr_status remap_build(const int32_t* lengths, int64_t n_seq, const int32_t* block_table,
                       int32_t blocks_per_seq, int32_t block_rows, int32_t tail_rows, int64_t cap,
                       int32_t* remap_out, int32_t* n_active_out, int32_t* n_runs_out) {

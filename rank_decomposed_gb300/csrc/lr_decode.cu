@@ -98,9 +98,21 @@ __device__ __forceinline__ void cluster_sync_all() {
 
 __device__ __forceinline__ float relu_f(float v) { return v > 0.0f ? v : 0.0f; }
 
+// Output row of token `tok`: the token itself, or its entry in the problem's
+// row list (-1 for an entry outside the output, which is reported).
+__device__ __forceinline__ int64_t out_row(const DecodeProblem& P, int tok) {
+  if (P.out_rows == nullptr) return tok;
+  const int64_t r = P.out_rows[tok];
+  if (r >= 0 && r < P.out_rows_limit) return r;
+  report_status(P.status, LR_ERR_REMAP_RANGE);
+  return -1;
+}
+
 // Four consecutive outputs (m, n .. n+3) of one problem.
 __device__ __forceinline__ void store_out4(const DecodeProblem& P, int m, int n, float4 v) {
-  const int64_t off = static_cast<int64_t>(m) * P.ldo + n;
+  const int64_t orow = out_row(P, m);
+  if (orow < 0) return;
+  const int64_t off = orow * P.ldo + n;
   if (P.epi == EPI_RELU_BF16) {
     v.x = relu_f(v.x); v.y = relu_f(v.y); v.z = relu_f(v.z); v.w = relu_f(v.w);
   }
@@ -144,7 +156,9 @@ __device__ __forceinline__ void store_staged_row(const DecodeProblem& P, int tok
                                                  const uint8_t* row) {
   const int esz = out_elem_bytes(P);
   const int rows = P.N - n0 < kTileN ? P.N - n0 : kTileN;
-  uint8_t* dst = static_cast<uint8_t*>(P.out) + (static_cast<int64_t>(tok) * P.ldo + n0) * esz;
+  const int64_t orow = out_row(P, tok);
+  if (orow < 0) return;
+  uint8_t* dst = static_cast<uint8_t*>(P.out) + (orow * P.ldo + n0) * esz;
   if (P.epi == EPI_ADD_F32)
     bulk_add_f32(dst, row, static_cast<uint32_t>(rows * esz));
   else
@@ -402,7 +416,22 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<NT>::kSlots)
         uint32_t r[16];
         tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, r);
         tmem_ld_wait();
-        if (n < P.N) {
+        if (n < P.N && P.out_rows != nullptr) {
+          // rows scattered through the problem's row list, one token at a time
+          const int nt = p.M - c * 16 < 16 ? p.M - c * 16 : 16;
+          for (int j = 0; j < nt; ++j) {
+            const int64_t orow = out_row(P, c * 16 + j);
+            if (orow < 0) continue;
+            const float v = __uint_as_float(r[j]);
+            if (epi_is_bf16(P.epi))
+              static_cast<uint16_t*>(P.out)[orow * P.ldo + n] =
+                  f32_to_bf16_rn(P.epi == EPI_RELU_BF16 ? relu_f(v) : v);
+            else if (P.epi == EPI_STORE_F32)
+              static_cast<float*>(P.out)[orow * P.ldo + n] = v;
+            else
+              static_cast<float*>(P.out)[orow * P.ldo + n] += v;
+          }
+        } else if (n < P.N) {
           const int nt = p.M - c * 16 < 16 ? p.M - c * 16 : 16;
           if (P.epi == EPI_ADD_F32) {
             float* o = static_cast<float*>(P.out) + n;
@@ -616,6 +645,9 @@ lr_status launch_nt(int M, const GemmOp* ops, int n_ops, int32_t* status, cudaSt
     P.out = o.out;
     P.ldo = o.ldo;
     P.vec_ok = (reinterpret_cast<uintptr_t>(o.out) % 16 == 0) && (o.ldo % 8 == 0) ? 1 : 0;
+    P.out_rows = o.out_rows;
+    P.out_rows_limit = o.out_rows_limit;
+    P.status = status;
     items += P.n_tiles * S;
   }
   cudaLaunchConfig_t cfg;

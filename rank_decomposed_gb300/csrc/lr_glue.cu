@@ -43,31 +43,48 @@ __device__ __forceinline__ int clamp_active(const int32_t* n_active, int64_t cap
   return n;
 }
 
+// Rows of the remap table one CTA copies.  Each warp copies whole rows with
+// 16-byte vectors, so a run of consecutive pool rows (the contiguous blocks of
+// the pages' scan) is read as one contiguous range, and rows of a few hundred
+// bytes (KV latents) do not cost a CTA each.
+constexpr int kCopyRows = 32;
+
 // buf[i] = pool[remap[i]] for i < n_active, zero rows otherwise.
 __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ pool, int64_t pool_rows,
                                                      int64_t row_vecs, const int32_t* __restrict__ remap,
                                                      const int32_t* __restrict__ n_active,
                                                      uint4* __restrict__ buf, int64_t cap,
                                                      int32_t* status) {
+  __shared__ int64_t src_row[kCopyRows];
   pdl_launch_dependents();
   pdl_wait();
-  const int64_t i = blockIdx.x;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kCopyRows;
   const int n = clamp_active(n_active, cap);
-  uint4* dst = buf + i * row_vecs;
-  const uint4* src = nullptr;
-  if (i < n) {
-    const int64_t j = remap[i];
-    if (j >= 0 && j < pool_rows) {
-      src = pool + j * row_vecs;
-    } else if (threadIdx.x == 0) {
-      report_status(status, LR_ERR_REMAP_RANGE);
+  if (threadIdx.x < kCopyRows) {
+    const int64_t i = i0 + threadIdx.x;
+    int64_t j = -1;
+    if (i < n) {
+      j = remap[i];
+      if (j < 0 || j >= pool_rows) {
+        report_status(status, LR_ERR_REMAP_RANGE);
+        j = -1;
+      }
     }
+    src_row[threadIdx.x] = j;
   }
-  if (src != nullptr) {
-    for (int64_t v = threadIdx.x; v < row_vecs; v += blockDim.x) dst[v] = src[v];
-  } else {
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int64_t v = threadIdx.x; v < row_vecs; v += blockDim.x) dst[v] = z;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows = cap - i0 < kCopyRows ? static_cast<int>(cap - i0) : kCopyRows;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int r = warp; r < rows; r += 8) {
+    uint4* dst = buf + (i0 + r) * row_vecs;
+    const int64_t j = src_row[r];
+    if (j >= 0) {
+      const uint4* src = pool + j * row_vecs;
+      for (int64_t v = lane; v < row_vecs; v += 32) dst[v] = src[v];
+    } else {
+      for (int64_t v = lane; v < row_vecs; v += 32) dst[v] = z;
+    }
   }
 }
 
@@ -78,19 +95,33 @@ __global__ void __launch_bounds__(256) scatter_kernel(const uint4* __restrict__ 
                                                       uint4* __restrict__ pool, int64_t pool_rows,
                                                       int64_t row_vecs, int64_t cap,
                                                       int32_t* status) {
+  __shared__ int64_t dst_row[kCopyRows];
   pdl_launch_dependents();
   pdl_wait();
-  const int64_t i = blockIdx.x;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kCopyRows;
   const int n = clamp_active(n_active, cap);
-  if (i >= n) return;
-  const int64_t j = remap[i];
-  if (j < 0 || j >= pool_rows) {
-    if (threadIdx.x == 0) report_status(status, LR_ERR_REMAP_RANGE);
-    return;
+  if (threadIdx.x < kCopyRows) {
+    const int64_t i = i0 + threadIdx.x;
+    int64_t j = -1;
+    if (i < n) {
+      j = remap[i];
+      if (j < 0 || j >= pool_rows) {
+        report_status(status, LR_ERR_REMAP_RANGE);
+        j = -1;
+      }
+    }
+    dst_row[threadIdx.x] = j;
   }
-  const uint4* src = buf + i * row_vecs;
-  uint4* dst = pool + j * row_vecs;
-  for (int64_t v = threadIdx.x; v < row_vecs; v += blockDim.x) dst[v] = src[v];
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows = cap - i0 < kCopyRows ? static_cast<int>(cap - i0) : kCopyRows;
+  for (int r = warp; r < rows; r += 8) {
+    const int64_t j = dst_row[r];
+    if (j < 0) continue;
+    const uint4* src = buf + (i0 + r) * row_vecs;
+    uint4* dst = pool + j * row_vecs;
+    for (int64_t v = lane; v < row_vecs; v += 32) dst[v] = src[v];
+  }
 }
 
 // out[m] = bf16(h[m] / sqrt(mean(h[m]^2) + eps)); one CTA per row.  Each
@@ -271,7 +302,8 @@ lr_status launch_gather(const void* pool, int64_t pool_rows, int64_t row_bytes,
                         const int32_t* remap, const int32_t* n_active, void* buf, int64_t cap,
                         int32_t* status, cudaStream_t s) {
   if (cap == 0) return LR_OK;
-  return launch(gather_kernel, dim3(static_cast<unsigned>(cap)), dim3(256), s, "gather",
+  return launch(gather_kernel, dim3(static_cast<unsigned>((cap + kCopyRows - 1) / kCopyRows)), dim3(256), s,
+                "gather",
                 static_cast<const uint4*>(pool), pool_rows, row_bytes / 16, remap, n_active,
                 static_cast<uint4*>(buf), cap, status);
 }
@@ -298,7 +330,8 @@ lr_status launch_scatter(const void* buf, const int32_t* remap, const int32_t* n
                          void* pool, int64_t pool_rows, int64_t row_bytes, int64_t cap,
                          int32_t* status, cudaStream_t s) {
   if (cap == 0) return LR_OK;
-  return launch(scatter_kernel, dim3(static_cast<unsigned>(cap)), dim3(256), s, "scatter",
+  return launch(scatter_kernel, dim3(static_cast<unsigned>((cap + kCopyRows - 1) / kCopyRows)), dim3(256), s,
+                "scatter",
                 static_cast<const uint4*>(buf), remap, n_active, static_cast<uint4*>(pool),
                 pool_rows, row_bytes / 16, cap, status);
 }

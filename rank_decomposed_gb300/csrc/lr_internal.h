@@ -49,6 +49,10 @@ struct GemmOp {
   int32_t epi;
   void* out;
   int64_t ldo;
+  // Output row of activation row m: m, or out_rows[m] when given (entries
+  // outside [0, out_rows_limit) are skipped and reported as LR_ERR_REMAP_RANGE).
+  const int32_t* out_rows;
+  int64_t out_rows_limit;
 };
 
 // --------------------------------------------------- device-side parameters
@@ -63,6 +67,9 @@ struct DecodeProblem {
   int32_t vec_ok;       // out 16-byte aligned and ldo % 8 == 0: vector stores
   void* out;
   int64_t ldo;
+  const int32_t* out_rows;  // see GemmOp
+  int64_t out_rows_limit;
+  int32_t* status;
 };
 
 struct DecodeParams {
@@ -88,7 +95,20 @@ struct PrefillParams {
   void* out;
   int64_t ldo;
   int32_t* status;
+  // Paged activations (blocks != nullptr): activation row 16 i + j is row j of
+  // block blocks[i] of a paged pool of pool_blocks 16-row blocks, for
+  // i < *n_blocks; later rows, and entries outside the pool, read as zeros
+  // (the latter also report LR_ERR_REMAP_RANGE).
+  const int32_t* blocks;
+  const int32_t* n_blocks;
+  int64_t pool_blocks;
+  // Output row of activation row m (see GemmOp).
+  const int32_t* out_rows;
+  int64_t out_rows_limit;
 };
+
+// Rows of a block of the paged latent pool.
+constexpr int kPageRows = 16;
 
 // ------------------------------------------------------------- host helpers
 void set_error(const char* fmt, ...);
@@ -124,6 +144,11 @@ int num_sms();
 lr_status launch_decode(int M, const GemmOp* ops, int n_ops, int32_t* status, cudaStream_t s);
 
 lr_status launch_prefill(int64_t M, const GemmOp& op, int32_t* status, cudaStream_t s);
+// The same GEMM with its activation rows read from a paged pool through a
+// block list (see PrefillParams); op.act is the pool, op.ld_act its row
+// stride, M = cap_blocks * 16.
+lr_status launch_prefill_paged(int64_t M, const GemmOp& op, const int32_t* blocks, const int32_t* n_blocks,
+                               int64_t pool_blocks, int32_t* status, cudaStream_t s);
 lr_status launch_rmsnorm(const float* h, void* out_bf16, int64_t M, int d, float eps,
                          cudaStream_t s);
 lr_status launch_silu_mul(const void* g, const void* u, void* out, int64_t M, int d,

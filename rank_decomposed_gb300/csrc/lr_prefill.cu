@@ -11,7 +11,12 @@
 //  * 4-stage ring of 48 KB stages (128x64 activation + 256x64 weight, 128-byte
 //    swizzle);
 //  * two 256-column fp32 accumulators in TMEM, so the epilogue of one tile
-//    overlaps the MMAs of the next.
+//    overlaps the MMAs of the next;
+//  * paged activations (KV reconstruction, English summary page section
+//    2.C): a 128-row activation tile is eight 16-row blocks of a paged pool,
+//    each loaded by its own TMA box at its block's row; a 16-row box lands on
+//    a 2 KB boundary, so the 128-byte swizzle of the stage is the same as
+//    that of one 128-row box.
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -99,11 +104,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_a = l2_policy_evict_last();
       const uint64_t pol_w = l2_policy_evict_last();
       pdl_wait();
+      const bool paged = p.blocks != nullptr;
+      const int nb = paged ? *reinterpret_cast<const volatile int32_t*>(p.n_blocks) : 0;
+      // paged: the block ids of a tile's eight blocks, loaded one tile ahead
+      constexpr int kTB = kBM / kPageRows;
+      int32_t bnext[kTB];
+      auto load_ids = [&](int t) {
+#pragma unroll
+        for (int j = 0; j < kTB; ++j) {
+          const int i = (t / p.n_tiles) * kTB + j;
+          bnext[j] = (t < tiles && i < nb && i * kPageRows < p.M) ? p.blocks[i] : -1;
+        }
+      };
+      if (paged) load_ids(blockIdx.x);
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         int m0, n0;
         tile_coords(p, t, m0, n0);
+        // paged: the pool row of each block (pool_blocks * 16, past the pool,
+        // for padding and bad entries: it reads as zeros)
+        int32_t brow[kTB];
+        if (paged) {
+#pragma unroll
+          for (int j = 0; j < kTB; ++j) {
+            int64_t b = bnext[j];
+            if (b >= p.pool_blocks || (b < 0 && m0 / kPageRows + j < nb && (m0 / kPageRows + j) * kPageRows < p.M)) {
+              report_status(p.status, LR_ERR_REMAP_RANGE);
+              b = -1;
+            }
+            brow[j] = static_cast<int32_t>((b < 0 ? p.pool_blocks : b) * kPageRows);
+          }
+          load_ids(t + gridDim.x);
+        }
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&empty_bar[s], ((it / kStages) & 1) ^ 1, &abort_sh)) {
@@ -114,7 +147,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* st = smem + s * kStageBytes;
           mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
-          tma_load_2d(st, &map_a, &full_bar[s], act_col(p, kb), m0, pol_a);
+          if (paged) {
+#pragma unroll
+            for (int j = 0; j < kBM / kPageRows; ++j)
+              tma_load_2d(st + j * kPageRows * kBK * 2, &map_a, &full_bar[s], kb * kBK, brow[j], pol_a);
+          } else {
+            tma_load_2d(st, &map_a, &full_bar[s], act_col(p, kb), m0, pol_a);
+          }
           tma_load_2d(st + kABytes, &map_w, &full_bar[s], kb * kBK, n0, pol_w);
         }
       }
@@ -190,8 +229,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r[16];
         tmem_ld16(tbase + c * 16, r);
         tmem_ld_wait();
-        if (m < p.M) {
-          const int64_t off = static_cast<int64_t>(m) * p.ldo + n;
+        int64_t orow = m < p.M ? m : -1;
+        if (orow >= 0 && p.out_rows != nullptr) {
+          orow = p.out_rows[m];
+          if (orow < 0 || orow >= p.out_rows_limit) {
+            if (c == 0) report_status(p.status, LR_ERR_REMAP_RANGE);
+            orow = -1;
+          }
+        }
+        if (orow >= 0) {
+          const int64_t off = orow * p.ldo + n;
           if (epi_is_bf16(p.epi)) {
             if (p.epi == EPI_RELU_BF16) {
 #pragma unroll
@@ -248,9 +295,13 @@ lr_status configure_prefill() {
   return LR_OK;
 }
 
-lr_status launch_prefill(int64_t M, const GemmOp& op, int32_t* status, cudaStream_t s) {
+lr_status launch_prefill_impl(int64_t M, const GemmOp& op, const int32_t* blocks, const int32_t* n_blocks,
+                              int64_t pool_blocks, int32_t* status, cudaStream_t s) {
   PrefillParams p;
   memset(&p, 0, sizeof(p));
+  p.blocks = blocks;
+  p.n_blocks = n_blocks;
+  p.pool_blocks = pool_blocks;
   p.M = static_cast<int32_t>(M);
   p.N = op.N;
   p.K = op.K;
@@ -262,8 +313,14 @@ lr_status launch_prefill(int64_t M, const GemmOp& op, int32_t* status, cudaStrea
   p.out = op.out;
   p.ldo = op.ldo;
   p.status = status;
+  p.out_rows = op.out_rows;
+  p.out_rows_limit = op.out_rows_limit;
   CUtensorMap ma, mw;
-  lr_status st = encode_map_bf16(&ma, op.act, static_cast<uint64_t>(M), op.act_cols, op.ld_act, kBM);
+  // paged: the map spans the pool, one 16-row block per box
+  lr_status st = blocks != nullptr
+                     ? encode_map_bf16(&ma, op.act, static_cast<uint64_t>(pool_blocks) * kPageRows, op.act_cols,
+                                       op.ld_act, kPageRows)
+                     : encode_map_bf16(&ma, op.act, static_cast<uint64_t>(M), op.act_cols, op.ld_act, kBM);
   if (st != LR_OK) return st;
   st = encode_map_bf16(&mw, op.W, op.N, op.K, op.ldw, kBN);
   if (st != LR_OK) return st;
@@ -287,6 +344,15 @@ lr_status launch_prefill(int64_t M, const GemmOp& op, int32_t* status, cudaStrea
   cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_kernel, p, ma, mw);
   if (e != cudaSuccess) return cuda_fail(e, "prefill: launch");
   return LR_OK;
+}
+
+lr_status launch_prefill(int64_t M, const GemmOp& op, int32_t* status, cudaStream_t s) {
+  return launch_prefill_impl(M, op, nullptr, nullptr, 0, status, s);
+}
+
+lr_status launch_prefill_paged(int64_t M, const GemmOp& op, const int32_t* blocks, const int32_t* n_blocks,
+                               int64_t pool_blocks, int32_t* status, cudaStream_t s) {
+  return launch_prefill_impl(M, op, blocks, n_blocks, pool_blocks, status, s);
 }
 
 }  // namespace lr

@@ -30,6 +30,22 @@ def assert_parity(y, y_ref, what=""):
     return worst / tol
 
 
+def assert_parity_bf16(y, y_ref, what=""):
+    """The parity bar for an output stored as bf16: the bar of the fp32 result
+    plus the rounding of the stored value (half an ulp is at most 2^-8 |y_ref|
+    relative).  Returns max|err| / bound."""
+    y = np.asarray(y, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    assert y.shape == y_ref.shape, (y.shape, y_ref.shape)
+    assert np.all(np.isfinite(y)), what + ": non-finite output"
+    bound = tol_of(y_ref) + 2.0 ** -8 * np.abs(y_ref)
+    ratio = np.abs(y - y_ref) / bound
+    worst = float(ratio.max()) if ratio.size else 0.0
+    assert worst <= 1.0, "%s: max err / bound %.3g (at %s)" % (
+        what, worst, np.unravel_index(int(ratio.argmax()), ratio.shape))
+    return worst
+
+
 def dev_bits(bits):
     """numpy uint16 bf16 bits -> torch bfloat16 CUDA tensor (same bits)."""
     import torch

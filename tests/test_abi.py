@@ -214,3 +214,36 @@ def test_factor_pack_argument_checks_launch_nothing():
     assert pack(A, B, 64, 64, 64, A + 4096, Bt) == lr.LR_ERR_INVALID_ARG
     assert pack(A, B, 64, 64, 64, At, At + 4096) == lr.LR_ERR_INVALID_ARG  # At and Bt overlap
     assert "overlap" in lr.last_error()
+
+
+@pytest.mark.parametrize("cap", [40, 200])
+def test_remap_build_blocks_matches_oracle(cap):
+    L, table, _ = synth.paged_batch(3, 12, 20, 300, 16)
+    if cap < sum((int(x) + 15) // 16 for x in L):
+        with pytest.raises(lr.LrError):
+            lr.remap_build_blocks(L, table, 16, cap)
+        return
+    got = lr.remap_build_blocks(L, table, 16, cap)
+    want = oracle.remap_build_blocks(L, table, 16, cap)
+    assert got[0].tolist() == want[0].tolist() and got[1:] == want[1:]
+
+
+def test_kv_reconstruct_paged_argument_checks_launch_nothing():
+    call = lambda r=64, d_kv=128, cap=4, pool=2, ptr=0x1000: lr.lib.lr_kv_reconstruct_paged(
+        ptr, pool, r, 0x2000, 0x3000, cap, 0x4000, d_kv, 0x5000, None, None)
+    assert call(cap=0) == lr.LR_OK
+    assert call(r=100) == lr.LR_ERR_UNSUPPORTED
+    assert call(r=0) == lr.LR_ERR_INVALID_ARG
+    assert call(ptr=0) == lr.LR_ERR_INVALID_ARG
+    assert call(ptr=0x1008) == lr.LR_ERR_INVALID_ARG
+    assert call(pool=1 << 28) == lr.LR_ERR_INVALID_ARG       # 2^32 rows overflow int32
+
+
+def test_kv_latent_write_argument_checks_launch_nothing():
+    call = lambda M=4, d_in=512, r=64, x=0x1000, ldx=512: lr.lib.lr_kv_latent_write(
+        x, ldx, M, 0x2000, d_in, r, 0x3000, 0x4000, 100, None, None)
+    assert call(M=0) == lr.LR_OK
+    assert call(r=100) == lr.LR_ERR_UNSUPPORTED
+    assert call(x=0) == lr.LR_ERR_INVALID_ARG
+    assert call(ldx=500) == lr.LR_ERR_INVALID_ARG
+    assert call(x=0x1004) == lr.LR_ERR_INVALID_ARG

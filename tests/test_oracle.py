@@ -354,6 +354,77 @@ def test_kv_reconstruct_identity_and_commutation():
     assert not np.any(out[9:])
 
 
+def test_remap_build_blocks_hand_example_and_rows():
+    """Block list of a hand-worked paged batch, and its agreement with the row-level scan.
+
+    Lengths 20, 3, 0, 33 with 16-row blocks need 2, 1, 0 and 3 blocks; their
+    table rows list the physical blocks in order.  Every listed row of
+    remap_build (all positions) is row p % 16 of the block that holds p.
+    """
+    lengths = [20, 3, 0, 33]
+    table = [[7, 2, -1], [5, -1, -1], [-1, -1, -1], [0, 1, 9]]
+    blocks, n, runs = oracle.remap_build_blocks(lengths, table, 16, 8)
+    assert blocks.tolist() == [7, 2, 5, 0, 1, 9, -1, -1]
+    assert n == 6
+    assert runs == 5           # 7 | 2 | 5 | 0,1 | 9
+    rows, nr, _ = oracle.remap_build(lengths, table, 16, 0, 64)
+    assert nr == sum(lengths)
+    i = 0
+    for s2, L in enumerate(lengths):
+        for p2 in range(L):
+            blk = int(table[s2][p2 // 16])
+            assert rows[i] == blk * 16 + p2 % 16
+            i += 1
+    with pytest.raises(ValueError):
+        oracle.remap_build_blocks(lengths, table, 16, 5)
+
+
+def test_kv_reconstruct_paged_matches_row_level():
+    """Per listed block the paged reconstruction equals the row-level one on the
+    sequence's positions; padding entries give zero rows; a bad id is flagged."""
+    pool_bits = synth.bf16_normal(6, 93, (10 * 16, 64))
+    pool = oracle.widen_bf16(pool_bits)
+    B = _bf16_matrix(6, 94, (64, 128), 0.125)
+    lengths, table = [20, 35], [[3, 8, -1], [1, 0, 6]]
+    blocks, n, _ = oracle.remap_build_blocks(lengths, table, 16, 7)
+    out, bad = oracle.kv_reconstruct_paged(pool, blocks, n, B)
+    assert not bad and out.shape == (7 * 16, 128)
+    rows, nr, _ = oracle.remap_build(lengths, table, 16, 0, 64)
+    _, ref, _ = oracle.kv_reconstruct(pool, rows, nr, 64, B)
+    i = 0
+    for s2, L in enumerate(lengths):
+        first = sum((lengths[t] + 15) // 16 for t in range(s2))
+        for p2 in range(L):
+            assert np.array_equal(out[(first + p2 // 16) * 16 + p2 % 16], ref[i])
+            i += 1
+    assert not np.any(out[n * 16:])
+    blocks[1] = 99
+    out2, bad = oracle.kv_reconstruct_paged(pool, blocks, n, B)
+    assert bad and not np.any(out2[16:32])
+
+
+def test_kv_latent_write_then_reconstruct():
+    """Writing the latents of new tokens into their pool rows and reconstructing
+    those rows gives the dense product x A B of the tokens, and the other rows
+    of the pool are untouched; an entry outside the pool is skipped and flagged."""
+    x = _bf16_matrix(7, 95, (3, 32))
+    A = _bf16_matrix(7, 96, (32, 16), 0.2)
+    B = _bf16_matrix(7, 97, (16, 24), 0.2)
+    pool = _bf16_matrix(7, 98, (20, 16))
+    rows = [17, 2, 9]
+    out, bad = oracle.kv_latent_write(x, A, rows, pool)
+    assert not bad
+    for m, j in enumerate(rows):
+        assert np.allclose(out[j], x[m] @ A, rtol=0, atol=1e-13)
+    keep = [i for i in range(20) if i not in rows]
+    assert np.array_equal(out[keep], pool[keep])
+    _, rec, _ = oracle.kv_reconstruct(out, rows, 3, 3, B)
+    _, dense = oracle.lowrank_linear(x, A, B)
+    assert np.allclose(rec, dense, rtol=0, atol=1e-12)
+    out2, bad = oracle.kv_latent_write(x, A, [17, 20, -1], pool)
+    assert bad and np.array_equal(np.delete(out2, 17, axis=0), np.delete(pool, 17, axis=0))
+
+
 def test_block_relu_mlp_path():
     """Non-GLU MLP with up = I and down = I: h2 = h1 + max(n2, 0); the gate factor is never read."""
     d = 16
