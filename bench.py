@@ -808,9 +808,17 @@ def main():
         per_step = w.stack.launch_count()
         sb = step_bytes(args.M, args.layers, m=model)
         achieved = sb / (ms * 1e-3) / 1e9
-        traffic = decode_traffic() if model.name == "llama7b" and args.M == 64 else None
+        # DRAM bytes of the decode kernel per step: the profiled per-launch traffic
+        # of the per-linear launches (7 projections x down/up, 2 layers) times the
+        # 14 such launches of every layer; the step's grouped launches move the
+        # same bytes.  Glue kernels are not counted.
+        per_launch = decode_traffic() if model.name == "llama7b" and args.M == 64 else None
+        traffic = None if per_launch is None else round(per_launch * 14 * args.layers)
         line["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                             "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": peak_kind,
+                            "traffic_note": "per step: DRAM read+write bytes of the decode kernel (ncu, "
+                                            "profiles/decode_kernel_traffic.txt) scaled from 2 layers; null "
+                                            "when the kernel source changed since the capture",
                             "kernel": "decode_kernel (tcgen05 swap-AB down/up projections) with the step's "
                                       "glue kernels, as replayed in the step's CUDA graph",
                             "timed": "CUDA events around the timed replays on the replay stream",
