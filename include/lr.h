@@ -396,6 +396,19 @@ const char* lr_last_error(void);
  * variable does. */
 void lr_test_stall_producer(int32_t on);
 
+/* Testing hook (no counterpart on the pages).  Prefill-size GEMMs (M > 256)
+ * take their 256-row bands in groups, all of a group's bands for one weight
+ * tile before the next; a prefill-size linear runs its down and up
+ * projections in one launch, the up-projection tiles of each group placed a
+ * number of groups (the lag) after that group's down-projection tiles and
+ * waiting for them.  lr_test_prefill_schedule(lag, group) fixes the lag (at
+ * most the number of groups) and the bands per group of later launches;
+ * 0 restores the automatic choice of either, and a negative lag runs the two
+ * projections as two launches.  It exists so tests can make
+ * the up projection wait and vary the order of the tiles; results do not
+ * depend on it.  Nothing else sets it, and no environment variable does. */
+void lr_test_prefill_schedule(int32_t lag, int32_t group);
+
 
 #ifdef __cplusplus
 }

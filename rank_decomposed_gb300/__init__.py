@@ -100,6 +100,7 @@ def _load():
         "lr_status_string": (ctypes.c_char_p, [i32]),
         "lr_last_error": (ctypes.c_char_p, []),
         "lr_test_stall_producer": (None, [i32]),
+        "lr_test_prefill_schedule": (None, [i32, i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

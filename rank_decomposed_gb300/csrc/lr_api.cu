@@ -61,6 +61,28 @@ bool pdl_enabled() {
   return on;
 }
 
+static std::atomic<int> g_prefill_lag{0};
+static std::atomic<int> g_prefill_group{0};
+
+int test_prefill_lag() { return g_prefill_lag.load(std::memory_order_relaxed); }
+int test_prefill_group() { return g_prefill_group.load(std::memory_order_relaxed); }
+
+bool prefill_pair_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("LR_PREFILL_PAIR");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
+bool prefill_fused_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("LR_PREFILL_FUSED");
+    return prefill_pair_enabled() && !(v && v[0] == '0');
+  }();
+  return on && g_prefill_lag.load(std::memory_order_relaxed) >= 0;
+}
+
 // cuTensorMapEncodeTiled, looked up once through the runtime so the library
 // needs no link-time dependency on the driver library.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -118,6 +140,8 @@ lr_status ensure_configured() {
   if (st != LR_OK) return st;
   st = configure_prefill();
   if (st != LR_OK) return st;
+  st = configure_prefill_pair();
+  if (st != LR_OK) return st;
   done[dev] = true;
   return LR_OK;
 }
@@ -174,7 +198,8 @@ lr_status run_ops(int64_t M, const GemmOp* ops, int n, int32_t* status, cudaStre
   if (cst != LR_OK) return cst;
   if (M <= kDecodeMaxRows) return launch_decode(static_cast<int>(M), ops, n, status, s);
   for (int i = 0; i < n; ++i) {
-    lr_status st = launch_prefill(M, ops[i], status, s);
+    lr_status st = prefill_pair_enabled() ? launch_prefill_pair(M, ops[i], status, s)
+                                          : launch_prefill(M, ops[i], status, s);
     if (st != LR_OK) return st;
   }
   return LR_OK;
@@ -197,6 +222,13 @@ lr_status enqueue_linear(const void* x, int64_t ldx, void* y, int64_t ldy, lr_dt
   GemmOp down = make_op(f->At, f->r, f->d_in, x, ldx, f->d_in, EPI_STORE_BF16, t, f->r);
   GemmOp up = make_op(f->Bt, f->d_out, f->r, t, f->r, f->r,
                       y_dtype == LR_BF16 ? EPI_STORE_BF16 : EPI_STORE_F32, y, ldy);
+  if (prefill_fuse_linear(M, down, up)) {
+    lr_status cst = ensure_configured();
+    if (cst != LR_OK) return cst;
+    int32_t* cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(t) +
+                                              align_up(static_cast<size_t>(M) * static_cast<size_t>(f->r) * 2));
+    return launch_prefill_pair_fused(M, down, up, cnt, status, s);
+  }
   lr_status st = run_ops(M, &down, 1, status, s);
   if (st != LR_OK) return st;
   return run_ops(M, &up, 1, status, s);
@@ -224,6 +256,7 @@ BlockLayout block_layout(int64_t M, const lr_block_desc* b) {
   L.g = take(m * b->d_ff * 2);
   L.u = take(m * b->d_ff * 2);
   L.a = take(m * b->d_ff * 2);
+  L.cnt = take(M > kDecodeMaxRows ? prefill_band_counter_bytes(M) : 0);
   L.total = off;
   return L;
 }
@@ -273,6 +306,7 @@ struct Step {
   void* dst = nullptr;
   int d = 0;
   float eps = 0.f;
+  int32_t* cnt = nullptr;  // GEMM: band counters for a fused prefill-size linear
 };
 
 Step gemm_step(std::initializer_list<GemmOp> ops) {
@@ -286,7 +320,7 @@ Step gemm_step(std::initializer_list<GemmOp> ops) {
 // then up group); h += LR_o(attn(v)); n2 = RMSNorm(h);
 // h += LR_down(silu(LR_gate(n2)) * LR_up(n2)) (ReLU variant: the ReLU is
 // applied in the up projection's epilogue).
-void block_steps(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws, std::vector<Step>& out) {
+void block_steps_of(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws, std::vector<Step>& out) {
   const BlockLayout L = block_layout(M, b);
   const int d = b->d_model, dff = b->d_ff;
   const lr_factor* f = b->f;
@@ -355,12 +389,44 @@ void block_steps(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws, std::
   out.push_back(gemm_step({make_op(fd.Bt, d, fd.r, t[LR_DOWN], fd.r, fd.r, EPI_ADD_F32, h, d)}));
 }
 
-// Enqueue steps in order.
+void block_steps(float* h, int64_t M, const lr_block_desc* b, uint8_t* ws, std::vector<Step>& out) {
+  const size_t first = out.size();
+  block_steps_of(h, M, b, ws, out);
+  int32_t* cnt = reinterpret_cast<int32_t*>(ws + block_layout(M, b).cnt);
+  for (size_t i = first; i < out.size(); ++i) out[i].cnt = cnt;
+}
+
+// A GEMM step followed by the GEMM step that reads each of its outputs as
+// activations: the down and up projections of the same linears.
+bool down_up_pair(const Step& a, const Step& b) {
+  if (a.kind != Step::GEMM || b.kind != Step::GEMM || a.n != b.n || a.cnt == nullptr) return false;
+  for (int j = 0; j < a.n; ++j)
+    if (b.ops[j].act != a.ops[j].out || b.ops[j].K != a.ops[j].N || a.ops[j].out_rows != nullptr)
+      return false;
+  return true;
+}
+
+// Enqueue steps in order.  At prefill sizes each down/up pair runs as one
+// fused launch per linear.
 lr_status enqueue_steps(const std::vector<Step>& steps, int64_t M, int32_t* status, cudaStream_t s) {
+  const bool prefill = M > kDecodeMaxRows && prefill_fused_enabled();
   for (size_t i = 0; i < steps.size(); ++i) {
     const Step& st = steps[i];
     lr_status r;
-    if (st.kind == Step::GEMM) {
+    if (prefill && i + 1 < steps.size() && down_up_pair(st, steps[i + 1])) {
+      r = ensure_configured();
+      for (int j = 0; j < st.n && r == LR_OK; ++j) {
+        const GemmOp& dn = st.ops[j];
+        const GemmOp& up = steps[i + 1].ops[j];
+        if (prefill_fuse_linear(M, dn, up)) {
+          r = launch_prefill_pair_fused(M, dn, up, st.cnt, status, s);
+        } else {
+          r = run_ops(M, &dn, 1, status, s);
+          if (r == LR_OK) r = run_ops(M, &up, 1, status, s);
+        }
+      }
+      ++i;
+    } else if (st.kind == Step::GEMM) {
       r = run_ops(M, st.ops, st.n, status, s);
     } else if (st.kind == Step::RMSNORM) {
       r = launch_rmsnorm(static_cast<const float*>(st.src0), st.dst, M, st.d, st.eps, s);
@@ -384,7 +450,9 @@ int64_t block_launches(int64_t M, const lr_block_desc* b) {
   // a silu_mul launch; ReLU is applied in the up projection's epilogue.
   const int64_t glu = b->mlp == LR_MLP_RELU ? 0 : 1;
   if (M <= kDecodeMaxRows) return 2 + glu + 8;
-  return 2 + glu + (b->mlp == LR_MLP_RELU ? 12 : 14);
+  // two launches per linear: down and up, or a counter-clearing launch and
+  // the fused launch
+  return 2 + glu + 2 * (b->mlp == LR_MLP_RELU ? 6 : 7);
 }
 
 // ---------------------------------------------------------------- stack
@@ -479,9 +547,16 @@ const char* lr_last_error(void) { return g_err; }
 
 void lr_test_stall_producer(int32_t on) { g_stall_producer.store(on != 0 ? 1 : 0); }
 
+void lr_test_prefill_schedule(int32_t lag, int32_t group) {
+  g_prefill_lag.store(lag > 0 ? lag : (lag < 0 ? -1 : 0));
+  g_prefill_group.store(group > 0 ? group : 0);
+}
+
 size_t lr_linear_workspace_bytes(int64_t M, const lr_factor* f) {
   if (f == nullptr || M < 0) return 0;
-  return align_up(static_cast<size_t>(M) * static_cast<size_t>(f->r) * 2);
+  size_t n = align_up(static_cast<size_t>(M) * static_cast<size_t>(f->r) * 2);
+  if (M > kDecodeMaxRows) n += align_up(prefill_band_counter_bytes(M));
+  return n;
 }
 
 lr_status lr_linear_forward(const void* x, int64_t ldx, void* y, int64_t ldy, lr_dtype y_dtype,

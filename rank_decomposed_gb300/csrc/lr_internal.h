@@ -144,6 +144,25 @@ int num_sms();
 lr_status launch_decode(int M, const GemmOp* ops, int n_ops, int32_t* status, cudaStream_t s);
 
 lr_status launch_prefill(int64_t M, const GemmOp& op, int32_t* status, cudaStream_t s);
+// The same GEMM on SM pairs (tcgen05 cta_group::2, 256 x 256 tiles).
+lr_status launch_prefill_pair(int64_t M, const GemmOp& op, int32_t* status, cudaStream_t s);
+// A prefill-size factorized linear in one launch on SM pairs: down (writes
+// T) and up (reads T) with band-ordered tiles.  band_done: device int32
+// [ceil(M / 256)], cleared by the call.
+lr_status launch_prefill_pair_fused(int64_t M, const GemmOp& down, const GemmOp& up, int32_t* band_done,
+                                    int32_t* status, cudaStream_t s);
+size_t prefill_band_counter_bytes(int64_t M);
+// Whether a linear of M rows with these down/up GEMMs runs as one fused
+// launch (prefill sizes only).
+bool prefill_fuse_linear(int64_t M, const GemmOp& down, const GemmOp& up);
+// Whether prefill-size GEMMs run on SM pairs (LR_PREFILL_PAIR=0 turns it
+// off) and whether a prefill-size linear is one fused launch
+// (LR_PREFILL_FUSED=0 turns it off); both read once.
+bool prefill_pair_enabled();
+bool prefill_fused_enabled();
+// Lag and band group fixed by lr_test_prefill_schedule (0: automatic).
+int test_prefill_lag();
+int test_prefill_group();
 // The same GEMM with its activation rows read from a paged pool through a
 // block list (see PrefillParams); op.act is the pool, op.ld_act its row
 // stride, M = cap_blocks * 16.
@@ -175,11 +194,12 @@ lr_status launch_scatter(const void* buf, const int32_t* remap, const int32_t* n
 // device; done once per device before the first launch or capture.
 lr_status configure_decode();
 lr_status configure_prefill();
+lr_status configure_prefill_pair();
 lr_status ensure_configured();
 
 // Buffers of one block inside its scratch (offsets in bytes, 256-aligned).
 struct BlockLayout {
-  size_t n1, t[7], q, k, v, n2, g, u, a, total;
+  size_t n1, t[7], q, k, v, n2, g, u, a, cnt, total;  // cnt: prefill band counters
 };
 BlockLayout block_layout(int64_t M, const lr_block_desc* b);
 

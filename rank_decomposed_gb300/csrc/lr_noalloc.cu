@@ -20,7 +20,8 @@
 namespace lr {
 namespace {
 
-// Size of the static scratch: t = x A_r in bf16 needs 2 * M * r bytes.
+// Size of the static scratch: t = x A_r in bf16 needs 2 * M * r bytes (and,
+// above 256 rows, the prefill band counters after it).
 constexpr size_t kNoAllocScratchBytes = LR_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -69,10 +70,10 @@ extern "C" lr_status lr_linear_forward_noalloc(const void* x, int64_t ldx, void*
   if (M == 0) return LR_OK;
   st = check_linear_io("linear_noalloc", x, ldx, y, ldy, y_dtype, M, f);
   if (st != LR_OK) return st;
-  const size_t need = static_cast<size_t>(M) * static_cast<size_t>(f->r) * 2;
+  const size_t need = lr_linear_workspace_bytes(M, f);
   if (need > kNoAllocScratchBytes) {
-    set_error("linear_noalloc: M * r * 2 = %zu bytes of scratch needed, the static array holds "
-              "%zu bytes (use lr_linear_forward with a workspace)",
+    set_error("linear_noalloc: %zu bytes of scratch needed (lr_linear_workspace_bytes), the static "
+              "array holds %zu bytes (use lr_linear_forward with a workspace)",
               need, kNoAllocScratchBytes);
     return LR_ERR_UNSUPPORTED;
   }
