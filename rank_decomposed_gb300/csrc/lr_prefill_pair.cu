@@ -16,7 +16,7 @@
 //  * the leader's commits arrive on the empty/accumulator-full barriers of
 //    both CTAs (multicast); the epilogue warps of both CTAs arrive on the
 //    leader's accumulator-empty barrier;
-//  * 6-stage ring of 32 KB stages, two 256-column fp32 accumulators.
+//  * 7-stage ring of 32 KB stages, two 256-column fp32 accumulators.
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -31,13 +31,11 @@ constexpr int kPM = 256;   // rows of a pair tile, 128 per CTA
 constexpr int kPN = 256;   // columns of a pair tile, split 128 / 128 between the CTAs
 constexpr int kHalf = 128;
 constexpr int kBK = 64;
-constexpr int kStages = 6;
+constexpr int kStages = 7;
 constexpr int kABytes = kHalf * kBK * 2;  // 16 KB: this CTA's activation rows
 constexpr int kBBytes = kHalf * kBK * 2;  // 16 KB: this CTA's weight rows
 constexpr int kStageBytes = kABytes + kBBytes;
-// 16 KB past the ring are never addressed by a load; they keep the last
-// stage's weight half well inside the allocation.
-constexpr int kSmem = kStages * kStageBytes + 16384 + 1024;
+constexpr int kSmem = kStages * kStageBytes + 1024;  // 225 KB with the alignment pad
 constexpr uint32_t kTmemCols = 512;  // two accumulators of 256 columns
 constexpr uint16_t kPairMask = 0x3;  // both CTAs of the cluster
 
