@@ -123,11 +123,15 @@ typedef struct {
  *   kept in `workspace`; the sums accumulate in fp32.  A bf16 y is the
  *   round-to-nearest-even image of the fp32 y.
  *   workspace: device, at least lr_linear_workspace_bytes(M, f) bytes, 256-byte
- *   aligned; its contents on entry do not matter (every element that is read
- *   was written by the same call).  Calls that share a workspace must be
+ *   aligned; it holds t (M x r bf16) and, for M > 256, one int32 completion
+ *   counter per 256-row band of the one-launch prefill form.  Its contents on
+ *   entry do not matter (every element that is read was written, or
+ *   cleared, by the same call).  Calls that share a workspace must be
  *   ordered on one stream.
  *   M = 0 is a no-op.  M <= 256 runs the decode kernels, larger M the prefill
- *   kernels.  The result is deterministic (no floating-point atomics). */
+ *   kernels (on SM pairs; a linear under 1.5e12 flops runs its down and up
+ *   projections in one launch).  The result is deterministic (no
+ *   floating-point atomics) and the same whichever form runs. */
 size_t lr_linear_workspace_bytes(int64_t M, const lr_factor* f);
 lr_status lr_linear_forward(const void* x, int64_t ldx, void* y, int64_t ldy, lr_dtype y_dtype,
                             int64_t M, const lr_factor* f, void* workspace, size_t ws_bytes,
@@ -148,9 +152,9 @@ lr_status lr_linear_forward(const void* x, int64_t ldx, void* y, int64_t ldy, lr
  *   call itself allocates nothing (no cudaMalloc/cudaFree, no allocating
  *   library routine).
  *   Arguments, layouts, checks and results are those of lr_linear_forward
- *   without the workspace.  M * r * 2 must not exceed LR_NOALLOC_SCRATCH_BYTES;
- *   larger problems are rejected with LR_ERR_UNSUPPORTED and a message in
- *   lr_last_error().
+ *   without the workspace.  lr_linear_workspace_bytes(M, f) (about M * r * 2)
+ *   must not exceed LR_NOALLOC_SCRATCH_BYTES; larger problems are rejected
+ *   with LR_ERR_UNSUPPORTED and a message in lr_last_error().
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress); make that first call before any stream capture.
  *   All calls share the one array and it keeps the last call's contents.
