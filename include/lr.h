@@ -391,8 +391,9 @@ const char* lr_last_error(void);
 
 /* ---------------------------------------------------------------------------
  * Testing hook (no counterpart on the pages).  lr_test_stall_producer(1) makes
- * the weight producer of every decode-size GEMM launched afterwards issue no
- * copy, so the bounded wait of the thread that consumes the copies runs out:
+ * the TMA producers of every decode-size GEMM and every SM-pair prefill GEMM
+ * launched afterwards issue no copy, so the bounded wait of the thread that
+ * consumes the copies runs out:
  * the launch reports LR_ERR_TIMEOUT through dev_status (after about two
  * seconds), releases its resources and returns, and the context stays usable.
  * lr_test_stall_producer(0) restores normal launches.  It exists for the

@@ -141,6 +141,7 @@ struct PairParams {
   PairGemm g[2];
   int32_t* band_done;
   int32_t* status;
+  int32_t stall_producer;  // fault-injection hook: the TMA producers issue nothing
 };
 
 struct Unit {
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && !p.stall_producer) {
       prefetch_tensormap(&map_a0);
       prefetch_tensormap(&map_w0);
       if (p.fused) {
@@ -558,6 +559,9 @@ lr_status launch_pair(const PairParams& p, const GemmOp* ops, int32_t* band_done
     ma[1] = ma[0];
     mw[1] = mw[0];
   }
+  PairParams q = p;
+  // Fault injection for the timeout path, set only through lr_test_stall_producer.
+  q.stall_producer = test_stall_producer() ? 1 : 0;
   if (p.fused) {
     // A kernel rather than a memset, so that the chain of programmatic
     // dependent launches is not broken.
@@ -597,7 +601,7 @@ lr_status launch_pair(const PairParams& p, const GemmOp* ops, int32_t* band_done
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel, p, ma[0], mw[0], ma[1], mw[1]);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel, q, ma[0], mw[0], ma[1], mw[1]);
   if (e != cudaSuccess) return cuda_fail(e, "prefill pair: launch");
   return LR_OK;
 }

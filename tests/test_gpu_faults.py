@@ -1,10 +1,12 @@
 """Failure detection without a GPU fault: bounded device waits report a status.
 
 The fault is injected on the host side of the launch: with the test hook
-lr_test_stall_producer set, the decode kernel's TMA producer issues no copy,
-so the MMA thread's wait on the first stage runs out (about two seconds).  The kernel must then report
-LR_ERR_TIMEOUT through the status word, release its resources and return, and
-the GPU must stay usable.
+lr_test_stall_producer set, the TMA producers of the decode kernel and of the
+paired-SM prefill kernel issue no copy, so the MMA thread's wait on the first
+stage runs out (about two seconds), and so do the epilogue waits of the other
+CTA of a pair.  The kernel must then report LR_ERR_TIMEOUT through the status
+word, release its resources (TMEM of both CTAs of a pair) and return, and the
+GPU must stay usable.
 """
 
 import numpy as np
@@ -28,18 +30,23 @@ def _linear(x, f, M):
     return y, int(st.item())
 
 
-@pytest.mark.parametrize("shape", [(512, 512, 64), (4096, 4096, 1216)])
-def test_bounded_wait_reports_timeout_and_gpu_recovers(shape):
+# M = 4: decode kernel; M = 300 and 1029: the paired-SM prefill kernel, as one
+# fused launch (its band waits never start) and, with the lag hook, as two
+@pytest.mark.parametrize("M,shape,two_launches", [(4, (512, 512, 64), False), (4, (4096, 4096, 1216), False),
+                                                  (300, (512, 1088, 192), False), (1029, (1024, 640, 320), True)])
+def test_bounded_wait_reports_timeout_and_gpu_recovers(M, shape, two_launches):
     d_in, d_out, r = shape
-    M = 4
     f = dev_factor(21, 0, 0, d_in, d_out, r)
     x_bits = synth.activations(21, M, d_in)
     x = dev_bits(x_bits)
+    if two_launches:
+        lr.lib.lr_test_prefill_schedule(-1, 0)
     lr.lib.lr_test_stall_producer(1)
     try:
         _, status = _linear(x, f, M)
     finally:
         lr.lib.lr_test_stall_producer(0)
+        lr.lib.lr_test_prefill_schedule(0, 0)
     assert status == lr.LR_ERR_TIMEOUT
     # the context is intact: the same call now succeeds and matches the oracle
     y, status = _linear(x, f, M)
