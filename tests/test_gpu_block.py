@@ -88,6 +88,31 @@ def test_block_llama70b_gqa_decode(M):
     assert_parity(out - h0, ref - h0, "70B block delta M=%d" % M)
 
 
+@pytest.mark.parametrize("cfg_name,M,seed", [("7b", 1029, 5), ("70b", 8192, 6)])
+def test_block_prefill_full_shapes_sampled_rows(cfg_name, M, seed):
+    """Full-size blocks at prefill sizes, checked on sampled rows (rows are independent).
+
+    7B shapes at 1029 rows: every linear runs as one fused launch.  70B-GQA
+    shapes at 8192 rows: the q/k/v/o linears are fused, the MLP linears (over
+    1.5e12 flops each) run as two launches; both feed the fp32 residual
+    through the add epilogue, and o reads the GQA-broadcast v.
+    """
+    cfg = LLAMA7B if cfg_name == "7b" else LLAMA70B
+    blk, host = make_layer(seed, 0, cfg)
+    bits, h0 = _h_input(seed, M, cfg["d"])
+    h = torch.from_numpy(h0.astype(np.float32)).cuda()
+    scratch = torch.zeros(lr.block_scratch_bytes(M, blk), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr.block_forward(h, blk, scratch, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, 511, M - 1],
+                                     synth.uniform_ints(seed, 9, 12, 0, M - 1)]))
+    ref = oracle.block_forward(h0[rows], host, cfg["n_heads"], cfg["n_kv"], cfg["hd"])
+    out = h[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
+    assert_parity(out - h0[rows], ref - h0[rows], "%s block at %d rows, sampled" % (cfg_name, M))
+
+
 def _make_stack(cfg, n_layers, cap, n_seq, seed=4, mode=0):
     layers, hosts = zip(*[make_layer(seed, l, cfg) for l in range(n_layers)])
     L, table, total = synth.paged_batch(seed, n_seq, 20, 300, 16)
