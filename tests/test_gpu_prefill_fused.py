@@ -111,3 +111,33 @@ def test_workspace_holds_band_counters():
     assert lr.linear_workspace_bytes(256, f) == al(256 * 64 * 2)
     assert lr.linear_workspace_bytes(257, f) == al(257 * 64 * 2) + al(4 * 2)
     assert lr.linear_workspace_bytes(16384, f) == al(16384 * 64 * 2) + al(4 * 64)
+
+
+@pytest.mark.parametrize("lag", [0, -1])
+@pytest.mark.parametrize("ydtype", [torch.float32, torch.bfloat16])
+def test_prefill_padded_leading_dimensions(lag_hook, lag, ydtype):
+    """Row strides wider than the rows: x with 64 extra columns, y with 8 (fused and two launches).
+
+    The padding columns of y are never written and every valid element matches the oracle
+    (bf16 y: the rounding of the fp32 y, which is what the oracle checks).
+    """
+    M, d_in, d_out, r = 777, 1024, 1216, 320
+    lag_hook(lag)
+    f = dev_factor(25, 0, 0, d_in, d_out, r)
+    A, B = host_factor(25, 0, 0, d_in, d_out, r)
+    x_bits = synth.bf16_normal(25, synth.make_tag(M, 0, synth.KIND_X), (M, d_in))
+    xf = torch.zeros((M, d_in + 64), dtype=torch.bfloat16, device="cuda")
+    xf[:, :d_in] = dev_bits(x_bits)
+    ws = torch.full((lr.linear_workspace_bytes(M, f),), 0xFF, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ys = {}
+    for dt in (torch.float32, ydtype):
+        yf = torch.full((M, d_out + 8), float("nan"), dtype=dt, device="cuda")
+        lr.linear_forward(xf[:, :d_in], f, yf[:, :d_out], ws, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert torch.isnan(yf[:, d_out:].float()).all()
+        ys[dt] = yf[:, :d_out]
+    want = oracle.lowrank_linear(oracle.widen_bf16(x_bits), A, B)[1]
+    assert_parity(ys[torch.float32].cpu().numpy(), want, "padded ld, lag %d" % lag)
+    assert torch.equal(ys[ydtype], ys[torch.float32].to(ydtype))
