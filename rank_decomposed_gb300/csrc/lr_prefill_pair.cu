@@ -9,8 +9,11 @@
 // memory; each CTA's TMEM receives its own 128 rows of the 256-column result.
 // Per SM this halves the weight bytes staged per k-block compared with a
 // 128 x 256 tile on one SM (32 KB instead of 48 KB a stage).
-//  * persistent: one pair per two SMs, pair tiles walked with the N tiles of
-//    one 256-row band adjacent (the band's activations come from L2);
+//  * persistent: one pair per two SMs, tiles taken in groups of 256-row
+//    bands, all of a group's bands for one weight tile before the next (see
+//    PairParams), so activations and weights are both re-read from L2;
+//  * a factorized linear can run as one launch: the down projection's tiles,
+//    then the up projection's, each waiting on per-band completion counters;
 //  * each CTA's producer loads its own halves, signalling the leader's
 //    full barrier (the leader alone arms it with both CTAs' bytes);
 //  * the leader's commits arrive on the empty/accumulator-full barriers of
@@ -132,8 +135,8 @@ struct PairGemm {
 // tiles of group s and, when fused, the second-GEMM tiles of group s - lag,
 // so that a group's T rows are read back while they are still in L2.
 // band_done[b] counts the epilogue warps that have stored a first-GEMM tile
-// of band b (8 per tile); a second-GEMM tile of band b starts loading once
-// it reaches 8 * g[0].n_tiles.
+// of band b (4 per CTA, 8 per pair tile); a second-GEMM tile of band b
+// starts loading once it reaches 8 * g[0].n_tiles.
 struct PairParams {
   int32_t M, m_tiles;  // m_tiles = ceil(M / 256) bands
   int32_t group, n_groups;
