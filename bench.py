@@ -600,7 +600,11 @@ def prefill_summary(res, model, M, tf):
             "M": M, "rho": 0.4, "tflops": main["tflops"], "frac_of_bf16_peak": main["frac_of_bf16_peak"],
             "ms_per_layer": main["ms_per_layer"],
             "tokens_per_s_all_layers": main["tokens_per_s_%d_layers" % model.layers],
-            "peak_tflops": tf, "sweep": sweep}
+            "peak_tflops": tf,
+            "kernel": "prefill_pair_kernel: tcgen05 cta_group::2 256x256 tiles on SM pairs; a linear under "
+                      "1.5e12 flops as one launch (down tiles, then up tiles), larger ones as two",
+            "timed": "CUDA events around the seven linears back to back, best of the repetitions",
+            "sweep": sweep}
 
 
 def config4(torch, lr, tf, steps):
