@@ -127,6 +127,34 @@ lr_status encode_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uin
   return LR_OK;
 }
 
+// A 3-D view of a bf16 [rows][cols] matrix whose columns are cut into chunks
+// of 64 (cols a multiple of 64): element (c, r, z) is [r][64 z + c].  A box of
+// {64, box_rows, box_chunks} then lands in shared memory as box_chunks
+// consecutive 128-byte-swizzled [box_rows][64] tiles: several k-blocks of a
+// K-major operand in one TMA operation.
+lr_status encode_map_bf16_chunks(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                                 uint64_t ld, uint32_t box_rows, uint32_t box_chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) {
+    set_error("cuTensorMapEncodeTiled unavailable");
+    return LR_ERR_CUDA;
+  }
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {ld * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, box_chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (3-D) failed (%d): rows=%llu cols=%llu ld=%llu box_rows=%u",
+              static_cast<int>(r), (unsigned long long)rows, (unsigned long long)cols,
+              (unsigned long long)ld, box_rows);
+    return LR_ERR_CUDA;
+  }
+  return LR_OK;
+}
+
 lr_status ensure_configured() {
   static bool done[64] = {false};
   static std::mutex mu;

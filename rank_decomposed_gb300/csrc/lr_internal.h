@@ -194,6 +194,10 @@ lr_status launch_scatter(const void* buf, const int32_t* remap, const int32_t* n
 // device; done once per device before the first launch or capture.
 lr_status configure_decode();
 lr_status configure_prefill();
+// A bf16 [rows][cols] matrix viewed as [cols / 64][rows][64]: one box of
+// {64, box_rows, box_chunks} loads box_chunks consecutive k-blocks.
+lr_status encode_map_bf16_chunks(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                                 uint64_t ld, uint32_t box_rows, uint32_t box_chunks);
 lr_status configure_prefill_pair();
 lr_status ensure_configured();
 

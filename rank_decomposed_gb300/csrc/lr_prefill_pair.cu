@@ -19,7 +19,10 @@
 //  * the leader's commits arrive on the empty/accumulator-full barriers of
 //    both CTAs (multicast); the epilogue warps of both CTAs arrive on the
 //    leader's accumulator-empty barrier;
-//  * 7-stage ring of 32 KB stages, two 256-column fp32 accumulators.
+//  * 3-stage ring of 64 KB stages, two k-blocks each, loaded by one 3-D TMA
+//    operation per operand (per-operation cost, not bytes in flight, was
+//    the limit of a 7-stage ring of single k-blocks); two 256-column fp32
+//    accumulators.
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -34,11 +37,13 @@ constexpr int kPM = 256;   // rows of a pair tile, 128 per CTA
 constexpr int kPN = 256;   // columns of a pair tile, split 128 / 128 between the CTAs
 constexpr int kHalf = 128;
 constexpr int kBK = 64;
-constexpr int kStages = 7;
-constexpr int kABytes = kHalf * kBK * 2;  // 16 KB: this CTA's activation rows
-constexpr int kBBytes = kHalf * kBK * 2;  // 16 KB: this CTA's weight rows
+constexpr int kKB = 2;       // k-blocks per stage, loaded by one TMA operation per operand
+constexpr int kStages = 3;
+constexpr int kSubBytes = kHalf * kBK * 2;   // 16 KB: one k-block of 128 rows
+constexpr int kABytes = kKB * kSubBytes;     // this CTA's activation rows
+constexpr int kBBytes = kKB * kSubBytes;     // this CTA's weight rows
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kSmem = kStages * kStageBytes + 1024;  // 225 KB with the alignment pad
+constexpr int kSmem = kStages * kStageBytes + 1024;  // 193 KB with the alignment pad
 constexpr uint32_t kTmemCols = 512;  // two accumulators of 256 columns
 constexpr uint16_t kPairMask = 0x3;  // both CTAs of the cluster
 
@@ -75,6 +80,16 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
       "l"(map), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// The same with a 3-D tensor map (chunked K; see encode_map_bf16_chunks).
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int32_t x, int32_t y, int32_t z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "l"(policy)
       : "memory");
 }
 
@@ -118,6 +133,7 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t mask) {
 struct PairGemm {
   int32_t N, K, n_tiles, epi;
   int32_t gqa_head_dim, gqa_group;
+  int32_t act_pairs;  // a stage's two activation k-blocks are adjacent chunks: one box
   void* out;
   int64_t ldo;
   const int32_t* out_rows;
@@ -317,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int arow = x.m0 + static_cast<int>(rank) * kHalf;
         const int wrow = x.n0 + static_cast<int>(rank) * (x.nt >> 1);
-        const int nkb = G.K / kBK;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int nst = (G.K / kBK + kKB - 1) / kKB;  // stages; the last may hold one k-block
+        for (int ks = 0; ks < nst; ++ks, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&empty_bar[s], ((it / kStages) & 1) ^ 1, &abort_sh)) {
             abort_sh = 1;
@@ -329,8 +345,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + s * kStageBytes;
           const uint32_t fb = peer_addr(smem_u32(&full_bar[s]), 0);
           if (leader) mbar_arrive_expect_tx(&full_bar[s], 2 * kStageBytes);
-          tma_load_2d_pair(st, ma, fb, act_col(G, kb), arow, pol);
-          tma_load_2d_pair(st + kABytes, mw, fb, kb * kBK, wrow, pol);
+          // (a k-block past K, in an odd last stage, reads zeros or unused data)
+          if (G.act_pairs) {
+            tma_load_3d_pair(st, ma, fb, 0, arow, act_col(G, kKB * ks) / kBK, pol);
+          } else {
+#pragma unroll
+            for (int h = 0; h < kKB; ++h)
+              tma_load_3d_pair(st + h * kSubBytes, ma, fb, 0, arow, act_col(G, kKB * ks + h) / kBK, pol);
+          }
+          tma_load_3d_pair(st + kABytes, mw, fb, 0, wrow, kKB * ks, pol);
         }
       }
       if (abort_sh) {
@@ -362,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit x = sched_unit(p, sc);
         const uint32_t idesc = idesc_bf16_f32(kPM, x.nt);
         const int nkb = p.g[x.g].K / kBK;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int nst = (nkb + kKB - 1) / kKB;
+        for (int ks = 0; ks < nst; ++ks, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&full_bar[s], (it / kStages) & 1, &abort_sh)) {
             ok = false;
@@ -370,11 +394,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * kStageBytes);
-          const uint64_t ad = smem_desc_sw128(sa);
-          const uint64_t bd = smem_desc_sw128(sa + kABytes);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            tc_mma_pair_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          for (int h = 0; h < kKB; ++h) {
+            if (kKB * ks + h >= nkb) break;
+            const uint64_t ad = smem_desc_sw128(sa + h * kSubBytes);
+            const uint64_t bd = smem_desc_sw128(sa + kABytes + h * kSubBytes);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              tc_mma_pair_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (ks | h | k) != 0 ? 1u : 0u);
+          }
           tc_commit_pair(&empty_bar[s], kPairMask);
         }
         tc_commit_pair(&accf_bar[b], kPairMask);
@@ -541,6 +569,8 @@ PairGemm pair_gemm(const GemmOp& op) {
   g.epi = op.epi;
   g.gqa_head_dim = op.gqa_head_dim;
   g.gqa_group = op.gqa_group;
+  // the head broadcast keeps k-blocks 2j, 2j+1 adjacent when a head spans whole pairs
+  g.act_pairs = (op.gqa_head_dim == 0 || op.gqa_head_dim % (kKB * kBK) == 0) ? 1 : 0;
   g.out = op.out;
   g.ldo = op.ldo;
   g.out_rows = op.out_rows;
@@ -552,10 +582,10 @@ lr_status launch_pair(const PairParams& p, const GemmOp* ops, int32_t* band_done
   const int n = p.fused ? 2 : 1;
   CUtensorMap ma[2], mw[2];
   for (int i = 0; i < n; ++i) {
-    lr_status st = encode_map_bf16(&ma[i], ops[i].act, static_cast<uint64_t>(p.M), ops[i].act_cols,
-                                   ops[i].ld_act, kHalf);
+    lr_status st = encode_map_bf16_chunks(&ma[i], ops[i].act, static_cast<uint64_t>(p.M), ops[i].act_cols,
+                                          ops[i].ld_act, kHalf, p.g[i].act_pairs ? kKB : 1);
     if (st != LR_OK) return st;
-    st = encode_map_bf16(&mw[i], ops[i].W, ops[i].N, ops[i].K, ops[i].ldw, kHalf);
+    st = encode_map_bf16_chunks(&mw[i], ops[i].W, ops[i].N, ops[i].K, ops[i].ldw, kHalf, kKB);
     if (st != LR_OK) return st;
   }
   if (n == 1) {
