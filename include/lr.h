@@ -176,7 +176,10 @@ lr_status lr_linear_forward_noalloc(const void* x, int64_t ldx, void* y, int64_t
  * section 2 "Generalizacion"; English page section 2.D (MHA/GQA/MQA, GLU MLP).
  * Linear inputs are rounded to bf16.  scratch: device, at least
  * lr_block_scratch_bytes(M, b) bytes, 256-byte aligned; its contents on entry
- * do not matter.  M = 0 is a no-op. */
+ * do not matter.  M = 0 is a no-op.  Each linear runs as lr_linear_forward
+ * would at the same M (decode kernels up to 256 rows, the SM-pair prefill
+ * GEMM above, one launch per linear below 1.5e12 flops); the result does not
+ * depend on which form runs. */
 size_t lr_block_scratch_bytes(int64_t M, const lr_block_desc* b);
 lr_status lr_block_forward(float* h, int64_t M, const lr_block_desc* b, void* scratch,
                            size_t scratch_bytes, int32_t* dev_status, lr_stream s);
